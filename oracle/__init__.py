@@ -1,0 +1,31 @@
+"""Plain, slow, fp64 CPU oracle of the future-attention-mass / pruned-cache path.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference leg may import it.  It shares no code with
+the CUDA library (``learned_kv_cache_gb300``) and neither imports the other; the
+seeded inputs come from ``kvp_inputs``.
+
+Functions and the passages they follow:
+
+* :func:`row_lse`, :func:`future_attn_mass` -- KVpop, "Defining Future
+  Attention Utility", "Delayed Memory Scoring" and Figure 2.
+* :func:`select_topk`, :func:`compact_kv` -- KVpop "The KVpop Scoring Module";
+  Learning to Evict from Key-Value Cache §1, §4.1, §A.2; How much KV cache can
+  you prune, "What we did" and "Conclusion".
+* :func:`decode_attn` -- How much KV cache can you prune, "Bounded windows".
+* :func:`soft_topk`, :func:`head_budgets` -- LKV, "The Differentiable Soft-TopK
+  Operator" and "LKV-H".
+
+Every function is pinned by the ``-m "not gpu"`` tests (brute force through
+library softmax/logsumexp on tiny inputs, closed forms, invariants and the
+pages' worked examples).
+"""
+from .attention_mass import future_attn_mass, row_lse
+from .budgets import head_budgets, soft_topk
+from .decode import decode_attn
+from .selection import compact_kv, effective_budget, select_row, select_topk
+
+__all__ = [
+    "row_lse", "future_attn_mass", "select_topk", "select_row", "effective_budget",
+    "compact_kv", "decode_attn", "soft_topk", "head_budgets",
+]
