@@ -1,0 +1,446 @@
+#!/usr/bin/env python3
+"""Benchmark of the future-attention-mass / pruned-cache hot path on GB300.
+
+One step = one pass of the whole path over the Qwen3-4B-shaped layer
+(32 query / 8 KV heads, head_dim 128, S = 8192, bf16, w = 128, 25 % budget,
+4 sinks + 128 recent): row LSE -> future-attention mass -> selection on F ->
+compaction -> one-token decode over the pruned cache.  Inputs are resident in
+HBM before the timed region; L2 is flushed (a 512 MiB write) before every
+timed step.  `value` is the algorithmic TFLOP/s of the two QK^T passes over
+the whole step time.  A second measured object, `decode`, is the pruned-cache
+decode of the Qwen2.5-1.5B-shaped decode-eviction workload (28 layers,
+12/2 heads, fp16, T = 120000 cache pruned to 4096) in GB/s.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload (the reference arm of this tier: there is no upstream code).
+Multi-GPU (torchrun): every rank runs its own independent layer (weak
+scaling, no data-path collective); timings are max-reduced over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import kvp_inputs  # noqa: E402
+
+METRIC = "future-attn-mass TFLOP/s (% bf16 peak); pruned-cache decode HBM GB/s (% peak)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic of one launch of the dominant kernel from an ncu capture, valid only while the
+# kernel source is unchanged (sha256 of the .cu file at capture time).
+NCU_TRAFFIC = {}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock / throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.out is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.out.seek(0)
+        rows = [r for r in csv.reader(io.StringIO(self.out.read())) if len(r) >= 9]
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm = float(r[1])
+                mx = float(r[2])
+                pw = float(r[3])
+            except ValueError:
+                continue
+            if pw > 200.0:       # under load
+                sms.append(sm)
+            for n, v in zip(names, r[5:9]):
+                if v.strip() == "Active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sms) if sms else None, "sm_max_mhz": mx,
+                "samples_under_load": len(sms), "reasons": sorted(reasons)}
+
+
+def file_sha(path):
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def oracle_sample_time(w, seconds_hint=None):
+    """The fp64 oracle on one query head of the workload's layer (LSE over all rows + F over
+    all keys): returns (flops, seconds, cores, description)."""
+    import oracle
+    x = kvp_inputs.make_prefill_layer(w, 0, device="cpu")
+    q = x["q"][:1]
+    k = x["k"][:1]
+    scale = w.head_dim ** -0.5
+    t0 = time.perf_counter()
+    lse = oracle.row_lse(q, k, scale)
+    oracle.future_attn_mass(q, k, lse, scale, w.window)
+    dt = time.perf_counter() - t0
+    S, ww = w.seq_len, max(w.seq_len - w.window, 0)
+    flops = 2.0 * w.head_dim * (S * (S + 1) // 2 + ww * (ww + 1) // 2)
+    desc = (f"one query head (of {w.h_q}) of the {w.name} layer: full causal row LSE and future "
+            f"mass over all {S} keys, fp64 numpy")
+    return flops, dt, os.cpu_count(), desc
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = kvp_inputs.QWEN3_4B_LAYER
+    for _ in range(args.warmup):
+        oracle_sample_time(w)
+    times = []
+    flops = 0.0
+    desc = ""
+    cores = os.cpu_count()
+    for _ in range(args.steps):
+        flops, dt, cores, desc = oracle_sample_time(w)
+        times.append(dt)
+    ms = 1e3 * sum(times) / len(times)
+    value = flops / (ms / 1e3) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "seq_len": w.seq_len, "h_q": w.h_q, "h_kv": w.h_kv,
+                   "head_dim": w.head_dim, "window": w.window, "sample": "one query head"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_kvp(args):
+    import learned_kv_cache_gb300 as kvp
+    from learned_kv_cache_gb300.pipeline import PrefillPrunePlan
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    kvp.load()
+    peaks, peak_src = load_peaks()
+    w = kvp_inputs.QWEN3_4B_LAYER
+    R, S, D = w.rows, w.seq_len, w.head_dim
+    x = kvp_inputs.make_prefill_layer(w.scaled(seed=w.seed + 100 * rank), 0, device=dev)
+    x = {k: v.unsqueeze(0).contiguous() for k, v in x.items()}
+    plan = PrefillPrunePlan(1, w.h_q, w.h_kv, S, D, x["q"].dtype, w.window, w.n_sink, w.n_recent,
+                            w.budget, device=dev)
+    budgets = torch.full((R,), w.budget, dtype=torch.int32, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def step(marks=None):
+        R_ = R
+
+        def mark(i):
+            if marks is not None:
+                marks[i].record(stream)
+        mark(0)
+        kvp.kvp_lse_pass(x["q"], x["k"], lse=plan.lse)
+        mark(1)
+        kvp.kvp_future_attn_mass(x["q"], x["k"], plan.lse, w.window, F=plan.F, workspace=plan.fam_ws)
+        mark(2)
+        kvp.kvp_select_topk(plan.F.view(R_, S), budgets, w.n_sink, w.n_recent, w.budget,
+                            idx=plan.idx, count=plan.count)
+        mark(3)
+        kvp.kvp_compact_kv(x["k"].view(R_, S, D), x["v"].view(R_, S, D), plan.idx, plan.count,
+                           k_out=plan.kc, v_out=plan.vc)
+        mark(4)
+        kvp.kvp_decode_attn(x["dq"], plan.kc, plan.vc, plan.count, out=plan.out,
+                            workspace=plan.dec_ws)
+        mark(5)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    kvp.kvp_check_device_status()
+
+    K = args.steps
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize(dev)
+        launches0 = kvp.kvp_launch_count()
+        t_wall = time.perf_counter()
+        for s in range(K):
+            flush.zero_()                      # evict L2 (not timed: outside the marks)
+            step(marks[s])
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall
+        launches = kvp.kvp_launch_count() - launches0
+        barrier()
+    kvp.kvp_check_device_status()
+    stage_names = ["lse_pass", "future_attn_mass", "select_topk", "compact_kv", "decode_attn"]
+    per_stage = {n: [] for n in stage_names}
+    step_ms = []
+    for m in marks:
+        for i, n in enumerate(stage_names):
+            per_stage[n].append(m[i].elapsed_time(m[i + 1]))
+        step_ms.append(m[0].elapsed_time(m[5]))
+    ms = sum(step_ms) / K
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    lse_flops = 2.0 * D * w.h_q * (S * (S + 1) // 2)
+    ww = S - w.window
+    fam_flops = 2.0 * D * w.h_q * (ww * (ww + 1) // 2)
+    flops = lse_flops + fam_flops
+    value = flops * ws / (ms / 1e3) / 1e12
+    stage_mean = {n: sum(v) / K for n, v in per_stage.items()}
+
+    # dominant kernel roofline
+    dom = "future_attn_mass" if stage_mean["future_attn_mass"] >= stage_mean["lse_pass"] else "lse_pass"
+    dom_flops = fam_flops if dom == "future_attn_mass" else lse_flops
+    achieved = dom_flops / (stage_mean[dom] / 1e3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    traffic = None
+    tc_src = os.path.join(ROOT, "learned_kv_cache_gb300", "csrc", "attn_mass_tc.cu")
+    simt_src = os.path.join(ROOT, "learned_kv_cache_gb300", "csrc", "attn_mass_simt.cu")
+    rec = NCU_TRAFFIC.get(dom)
+    if rec and rec.get("sha") in (file_sha(tc_src), file_sha(simt_src)):
+        traffic = rec["bytes"]
+    roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"{peak_src} bf16_tflops (burst)"}
+
+    # pruned-cache decode on the decode-eviction workload (HBM bound)
+    decode = decode_eviction_measure(kvp, dev, K, args.warmup, flush, peaks, ws)
+
+    # end to end through the public API with host buffers
+    e2e = e2e_measure(kvp, x, plan, budgets, w, K, args.warmup, stream, flops, ws, dev)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        f_c, t_c, cores, desc = oracle_sample_time(w)
+        cpu = {"value": f_c / t_c / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": desc, "seconds": t_c}
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "global_batch": ws, "seq_len": S, "h_q": w.h_q,
+                   "h_kv": w.h_kv, "head_dim": D, "window": w.window, "budget": w.budget,
+                   "n_sink": w.n_sink, "n_recent": w.n_recent,
+                   "l2": "flushed before every timed step (512 MiB write)",
+                   "parallelism": f"replicas: one independent layer per GPU x{ws}"},
+        "frac_of_bf16_peak": value / peak,
+        "stages_ms": stage_mean,
+        "roofline": roofline,
+        "decode": decode,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "wall_s_timed_region": t_wall,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def decode_eviction_measure(kvp, dev, K, W, flush, peaks, ws):
+    """Qwen2.5-1.5B decode eviction at T = 120000: control decode with key mass, select to 4096,
+    compact, pruned decode; the pruned decode's HBM GB/s is the reported figure."""
+    w = kvp_inputs.QWEN25_15B_DECODE
+    b = max(w.decode_budgets)
+    x = kvp_inputs.make_decode_cache(w, device=dev)
+    R, T, D = w.rows, w.seq_len, w.head_dim
+    full_len = torch.full((R,), T, dtype=torch.int32, device=dev)
+    mass = torch.empty(R, T, device=dev)
+    budgets = torch.full((R,), b, dtype=torch.int32, device=dev)
+    idx = torch.empty(R, b, dtype=torch.int32, device=dev)
+    cnt = torch.empty(R, dtype=torch.int32, device=dev)
+    kc = torch.empty(R, b, D, dtype=x["k"].dtype, device=dev)
+    vc = torch.empty_like(kc)
+    out_full = torch.empty(w.n_layers, w.h_q, D, device=dev)
+    out = torch.empty_like(out_full)
+    ws_full = torch.empty(kvp.kvp_decode_attn_workspace_size(w.n_layers, w.h_q, w.h_kv, D, T, True),
+                          dtype=torch.uint8, device=dev)
+    ws_pr = torch.empty(kvp.kvp_decode_attn_workspace_size(w.n_layers, w.h_q, w.h_kv, D, b, False),
+                        dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        kvp.kvp_decode_attn(x["q"], x["k"], x["v"], full_len, out=out_full, key_mass=mass,
+                            workspace=ws_full)
+        if ev:
+            ev[1].record(stream)
+        kvp.kvp_select_topk(mass, budgets, w.n_sink, w.n_recent, b, idx=idx, count=cnt)
+        if ev:
+            ev[2].record(stream)
+        kvp.kvp_compact_kv(x["k"], x["v"], idx, cnt, k_out=kc, v_out=vc)
+        if ev:
+            ev[3].record(stream)
+        flush.zero_()
+        if ev:
+            ev[4].record(stream)
+        kvp.kvp_decode_attn(x["q"], kc, vc, cnt, out=out, workspace=ws_pr)
+        if ev:
+            ev[5].record(stream)
+
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for s in range(K):
+        flush.zero_()
+        step(evs[s])
+    torch.cuda.synchronize(dev)
+    kvp.kvp_check_device_status()
+    t_full = sum(e[0].elapsed_time(e[1]) for e in evs) / K
+    t_sel = sum(e[1].elapsed_time(e[2]) for e in evs) / K
+    t_cmp = sum(e[2].elapsed_time(e[3]) for e in evs) / K
+    t_dec = sum(e[4].elapsed_time(e[5]) for e in evs) / K
+    elt = x["k"].element_size()
+    dec_bytes = 2 * R * b * D * elt + x["q"].numel() * elt + out.numel() * 4
+    full_bytes = 2 * R * T * D * elt + mass.numel() * 4
+    cmp_bytes = 4 * R * b * D * elt + R * b * 4
+    sel_bytes = R * T * 4 + R * b * 4
+    hbm = float(peaks["hbm_gbs"])
+    gbs = dec_bytes / (t_dec / 1e3) / 1e9
+    return {
+        "workload": w.name, "budget": b, "metric": "pruned-cache decode HBM GB/s",
+        "value": gbs, "unit": "GB/s", "frac": gbs / hbm, "peak": hbm,
+        "ms": t_dec, "bytes": dec_bytes, "l2": "flushed before the pruned decode",
+        "other_stages": {
+            "full_cache_decode_with_key_mass": {"ms": t_full, "GB/s": full_bytes / (t_full / 1e3) / 1e9},
+            "select_topk": {"ms": t_sel, "GB/s": sel_bytes / (t_sel / 1e3) / 1e9},
+            "compact_kv": {"ms": t_cmp, "GB/s": cmp_bytes / (t_cmp / 1e3) / 1e9},
+        },
+    }
+
+
+def e2e_measure(kvp, x, plan, budgets, w, K, W, stream, flops, ws, dev):
+    """Whole step through the public API from pinned host buffers: H2D of Q/K/V and the decode
+    query, the five stages, D2H of F, the kept indices/counts and the decode output."""
+    R, S, D = w.rows, w.seq_len, w.head_dim
+    host = {k: v.cpu().pin_memory() for k, v in x.items()}
+    dx = {k: torch.empty_like(v) for k, v in x.items()}
+    outs = {"F": plan.F, "idx": plan.idx, "count": plan.count, "out": plan.out}
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def step():
+        for k in dx:
+            dx[k].copy_(host[k], non_blocking=True)
+        kvp.kvp_lse_pass(dx["q"], dx["k"], lse=plan.lse)
+        kvp.kvp_future_attn_mass(dx["q"], dx["k"], plan.lse, w.window, F=plan.F,
+                                 workspace=plan.fam_ws)
+        kvp.kvp_select_topk(plan.F.view(R, S), budgets, w.n_sink, w.n_recent, w.budget,
+                            idx=plan.idx, count=plan.count)
+        kvp.kvp_compact_kv(dx["k"].view(R, S, D), dx["v"].view(R, S, D), plan.idx, plan.count,
+                           k_out=plan.kc, v_out=plan.vc)
+        kvp.kvp_decode_attn(dx["dq"], plan.kc, plan.vc, plan.count, out=plan.out,
+                            workspace=plan.dec_ws)
+        for k in outs:
+            host_out[k].copy_(outs[k], non_blocking=True)
+
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / K
+    return {"value": flops * ws / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="kvp", choices=["kvp", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_kvp(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,216 @@
+/*
+ * kvp.h -- C ABI of the future-attention-mass / pruned-KV-cache hot path (sm_103a).
+ *
+ * Five stages, one entry point each, plus the head-wise budget helper:
+ *
+ *   kvp_lse_pass           causal row log-sum-exp of the attention logits
+ *   kvp_future_attn_mass   transposed (key-major) pass: future-attention mass per key
+ *   kvp_soft_topk_budgets  closed-form Soft-TopK head ratios and budgets b = floor(r * t)
+ *   kvp_select_topk        sinks + recent window + top-k fill under per-row budgets
+ *   kvp_compact_kv         gather of the kept K/V rows into a dense pruned cache
+ *   kvp_decode_attn        one-token decode attention over the (pruned) cache
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every pointer argument is a DEVICE pointer unless stated otherwise; the
+ *   caller owns all buffers.  The library never allocates, frees or
+ *   synchronises (except kvp_check_device_status, which synchronises the given
+ *   stream).  Work is enqueued asynchronously on `stream` (a cudaStream_t;
+ *   NULL = the legacy default stream).
+ * - Arguments are validated on the host before anything is launched; a call
+ *   that returns an error has enqueued nothing.  Errors that only the device
+ *   can see (an out-of-range index or budget in a device array, a bounded wait
+ *   that gave up) are recorded in a per-device status word that
+ *   kvp_check_device_status() reads and clears; the affected outputs are then
+ *   unspecified.
+ * - Tensors are dense and row-major with the last dimension contiguous; the
+ *   layout of each argument is given in brackets.  Q/K/V base pointers must be
+ *   16-byte aligned.
+ * - head_dim must be 64 or 128.  Logits are scaled by `sm_scale` (normally
+ *   1/sqrt(head_dim)); all softmax arithmetic is fp32.
+ * - GQA: query head h_q belongs to KV head h_q / (h_q_count / h_kv_count).
+ */
+#ifndef KVP_H
+#define KVP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVP_ABI_VERSION 1
+
+/* A cudaStream_t (struct CUstream_st*), declared without pulling in CUDA headers. */
+typedef struct CUstream_st* kvp_stream_t;
+
+typedef enum kvp_dtype {
+  KVP_F32 = 0,  /* float32 */
+  KVP_BF16 = 1, /* bfloat16 */
+  KVP_F16 = 2   /* IEEE half */
+} kvp_dtype;
+
+typedef enum kvp_status {
+  KVP_OK = 0,
+  KVP_ERR_INVALID_ARG = -1,   /* null pointer, bad size, misaligned buffer, ... */
+  KVP_ERR_UNSUPPORTED = -2,   /* dtype / head_dim / layout this build does not handle */
+  KVP_ERR_CUDA = -3,          /* a CUDA runtime call failed; see kvp_last_error() */
+  KVP_ERR_TIMEOUT = -4,       /* device status: a bounded wait inside a kernel gave up */
+  KVP_ERR_WORKSPACE = -5,     /* workspace pointer null or smaller than the size query */
+  KVP_ERR_DEVICE_CHECK = -6   /* device status: a device-side index/budget was out of range */
+} kvp_status;
+
+/* ---------------------------------------------------------------------------
+ * A1. Causal row log-sum-exp.
+ *
+ * KVpop -- Key-Value Cache Compression with Predictive Online Pruning,
+ * "Delayed Memory Scoring" (worked LSE example) and Figure 2: the per-query
+ * log-normaliser that attention kernels return as their auxiliary LSE.
+ *
+ *   lse[b, h, i] = ln sum_{j <= i} exp(sm_scale * q[b, h, i, :] . k[b, h / G, j, :])
+ *
+ * q   [n_batch, h_q,  seq_len, head_dim]  dtype
+ * k   [n_batch, h_kv, seq_len, head_dim]  dtype
+ * lse [n_batch, h_q,  seq_len]            float32, natural log (output)
+ * n_batch counts independent problems (e.g. layers).  bf16/f16 inputs run on
+ * the tensor cores (fp32 accumulation); float32 inputs on fp32 FFMA.
+ * ------------------------------------------------------------------------- */
+int kvp_lse_pass(const void* q, const void* k, int dtype, int n_batch, int h_q, int h_kv,
+                 int seq_len, int head_dim, float sm_scale, float* lse, kvp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * A2. Future-attention mass (transposed, key-major column pass).
+ *
+ * KVpop, "Defining Future Attention Utility", "Delayed Memory Scoring" and
+ * Figure 2: the attention mass key j receives from the queries that have
+ * left the protected window (i >= j + window), obtained by swapping the roles
+ * of queries and keys and offsetting each logit by the query's LSE; summed
+ * over the GQA group of the KV head (raw sum: no count normalisation, no log):
+ *
+ *   F[b, h, j] = sum_{g < G} sum_{i = j + window}^{seq_len - 1}
+ *                exp(sm_scale * q[b, h*G+g, i] . k[b, h, j] - lse[b, h*G+g, i])
+ *
+ * The S x S matrix is never formed.  Keys j > seq_len - 1 - window get 0.
+ * q, k as in kvp_lse_pass; lse is kvp_lse_pass's output.
+ * F [n_batch, h_kv, seq_len] float32 (output).
+ * workspace: device scratch of at least kvp_future_attn_mass_workspace_size()
+ * bytes (partial sums of long key rows; may be NULL when that size is 0).
+ * ------------------------------------------------------------------------- */
+size_t kvp_future_attn_mass_workspace_size(int dtype, int n_batch, int h_q, int h_kv,
+                                           int seq_len, int head_dim, int window);
+int kvp_future_attn_mass(const void* q, const void* k, const float* lse, int dtype, int n_batch,
+                         int h_q, int h_kv, int seq_len, int head_dim, float sm_scale,
+                         int window, float* F, void* workspace, size_t workspace_bytes,
+                         kvp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * A0. Head-wise budgets from the closed-form Soft-TopK.
+ *
+ * LKV: End-to-End Learning of Head-wise Budgets and Token Selection for LLM
+ * KV Cache Eviction, "The Differentiable Soft-TopK Operator" (threshold
+ * lambda in closed form over the descending-sorted scores) and "LKV-H"
+ * (ratios r = ST_k(s) over the flattened head scores, budget b = floor(r*t)).
+ * Each ratio is the Laplace CDF of (s_i - lambda), the map whose budget
+ * equation sum_i r_i = k solves to the printed threshold; sum_i r_i = k.
+ *
+ * scores  [n] float64;  ratios [n] float64 (output);  budgets [n] int32 (output).
+ * Requires 1 <= n <= 1024, 0 < k < n, t >= 0, scores finite with |s| < 700.
+ * ------------------------------------------------------------------------- */
+int kvp_soft_topk_budgets(const double* scores, int n, double k, int t, double* ratios,
+                          int32_t* budgets, kvp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * A3. Budgeted per-row selection.
+ *
+ * KVpop, "The KVpop Scoring Module" and Figure 1 (sink tokens and a
+ * protected recent window are always kept; the top-k scores fill the rest of
+ * the fixed budget: 2 + 3 + 4 = 9 = B in its example); Learning to Evict from
+ * Key-Value Cache, §1 and §A.2 (discard the lowest-ranked entries to meet the
+ * budget; first four and last 16 always kept); How much KV cache can you
+ * prune, "What we did" (keep the first four, the newest 32, fill the rest).
+ *
+ * For each row r of scores [R, row_stride] (first T entries used):
+ *   b_eff = T if T <= b[r], else max(b[r], n_sink + n_recent);
+ *   keep [0, n_sink) and [T - n_recent, T), then the k = b_eff - n_sink - n_recent
+ *   highest scores of the middle, ties to the LOWER index, -0.0 == +0.0,
+ *   NaN below -inf.
+ * budgets [R] int32 (device);  idx [R, b_max] int32 (output): kept token
+ * indices in ascending order, padded with -1;  count [R] int32 (output) = b_eff.
+ * A row whose b_eff exceeds b_max (or whose budget is negative) gets
+ * count = -1 and raises KVP_ERR_DEVICE_CHECK in the device status.
+ * ------------------------------------------------------------------------- */
+int kvp_select_topk(const float* scores, int R, int T, int64_t row_stride,
+                    const int32_t* budgets, int n_sink, int n_recent, int32_t* idx,
+                    int b_max, int32_t* count, kvp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * A4. Compaction of the kept entries into a dense pruned cache.
+ *
+ * Learning to Evict from Key-Value Cache, §4.1 (chunked prefill-compress with
+ * physical tensor compaction); How much KV cache can you prune, "Conclusion"
+ * (the kept entries are copied into a new tensor).  Byte copy:
+ *
+ *   k_out[r, m, :] = k[r, idx[r, m], :],  v_out likewise,  for m < count[r]
+ *
+ * k, v [R, T, head_dim] dtype;  idx [R, b_max], count [R] from kvp_select_topk;
+ * k_out, v_out [R, b_max, head_dim] dtype (output; rows m >= count[r] are
+ * not written).  An index outside [0, T) raises KVP_ERR_DEVICE_CHECK.
+ * ------------------------------------------------------------------------- */
+int kvp_compact_kv(const void* k, const void* v, int dtype, int R, int T, int head_dim,
+                   const int32_t* idx, const int32_t* count, int b_max, void* k_out,
+                   void* v_out, kvp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * A5. Single-token decode attention over a (pruned) cache, split along keys.
+ *
+ * How much KV cache can you prune, "What we did" and "Bounded windows"
+ * (one-token attention over the retained entries); KVpop Figure 1
+ * (attention is computed over the retained set):
+ *
+ *   out[l, h, :] = sum_{m < len[r]} softmax_m(sm_scale * q[l, h] . kc[r, m]) vc[r, m],
+ *   r = l * h_kv + h / G;  len[r] = 0 gives a zero output.
+ *
+ * q [n_layers, h_q, head_dim] dtype;  kc, vc [n_layers*h_kv, T_cap, head_dim] dtype;
+ * len [n_layers*h_kv] int32 (device, each in [0, T_cap], else
+ * KVP_ERR_DEVICE_CHECK);  out [n_layers, h_q, head_dim] float32 (output).
+ * Optional key mass (key_mass != NULL): the probability each retained key
+ * receives, summed over the group's query heads (the cumulative past-attention
+ * score of the attention-score policy in How much KV cache can you prune), is
+ * written (accumulate = 0: the whole [R, T_src] array is overwritten, zeros
+ * where no retained key maps) or added (accumulate = 1) to
+ * key_mass [R, T_src] float32 at position key_pos[r, m] ([R, T_cap] int32,
+ * in [0, T_src)) or at m when key_pos is NULL (then T_src >= T_cap).
+ * Requires G = h_q / h_kv <= 8.
+ * workspace: at least kvp_decode_attn_workspace_size() bytes.
+ * ------------------------------------------------------------------------- */
+size_t kvp_decode_attn_workspace_size(int n_layers, int h_q, int h_kv, int head_dim, int T_cap,
+                                      int with_key_mass);
+int kvp_decode_attn(const void* q, const void* kc, const void* vc, int dtype, int n_layers,
+                    int h_q, int h_kv, int head_dim, int T_cap, const int32_t* len,
+                    float sm_scale, float* out, float* key_mass, const int32_t* key_pos,
+                    int T_src, int accumulate, void* workspace, size_t workspace_bytes,
+                    kvp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Status and diagnostics.
+ * ------------------------------------------------------------------------- */
+/* Static string for a kvp_status code. */
+const char* kvp_status_string(int status);
+/* Message of the last failing call on this host thread ("" if none). */
+const char* kvp_last_error(void);
+/* Synchronises `stream`, then reads and clears the current device's status
+ * word: KVP_OK, KVP_ERR_TIMEOUT or KVP_ERR_DEVICE_CHECK (first error recorded
+ * since the last read), or KVP_ERR_CUDA if the synchronisation failed. */
+int kvp_check_device_status(kvp_stream_t stream);
+/* KVP_ABI_VERSION of the loaded library. */
+int kvp_abi_version(void);
+/* Number of kernels this process has launched through the library so far
+ * (host-side counter, for accounting in benchmarks). */
+uint64_t kvp_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVP_H */

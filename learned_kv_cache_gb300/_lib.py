@@ -1,0 +1,276 @@
+"""ctypes binding of libkvp.so: the C ABI of include/kvp.h under the same names.
+
+Argument marshalling only: every function checks tensor devices, dtypes,
+shapes and contiguity, passes raw device pointers and the current CUDA stream
+to the library, and raises :class:`KvpError` on a non-zero status.  All
+arithmetic runs in the library's CUDA kernels; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkvp.so")
+
+KVP_F32, KVP_BF16, KVP_F16 = 0, 1, 2
+_DTYPE = {torch.float32: KVP_F32, torch.bfloat16: KVP_BF16, torch.float16: KVP_F16}
+
+STATUS = {0: "KVP_OK", -1: "KVP_ERR_INVALID_ARG", -2: "KVP_ERR_UNSUPPORTED", -3: "KVP_ERR_CUDA",
+          -4: "KVP_ERR_TIMEOUT", -5: "KVP_ERR_WORKSPACE", -6: "KVP_ERR_DEVICE_CHECK"}
+
+# Exported symbols and their C signatures (restype, argtypes), mirroring include/kvp.h.
+_P, _I, _F, _D, _SZ, _I64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_double,
+                             ctypes.c_size_t, ctypes.c_int64)
+SIGNATURES = {
+    "kvp_lse_pass": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P]),
+    "kvp_future_attn_mass_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "kvp_future_attn_mass": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _SZ, _P]),
+    "kvp_soft_topk_budgets": (_I, [_P, _I, _D, _I, _P, _P, _P]),
+    "kvp_select_topk": (_I, [_P, _I, _I, _I64, _P, _I, _I, _P, _I, _P, _P]),
+    "kvp_compact_kv": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P]),
+    "kvp_decode_attn_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "kvp_decode_attn": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _F, _P, _P, _P, _I, _I, _P,
+                             _SZ, _P]),
+    "kvp_status_string": (ctypes.c_char_p, [_I]),
+    "kvp_last_error": (ctypes.c_char_p, []),
+    "kvp_check_device_status": (_I, [_P]),
+    "kvp_abi_version": (_I, []),
+    "kvp_launch_count": (ctypes.c_uint64, []),
+}
+
+
+class KvpError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: {STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libkvp.so (raises if it has not been built: there is no fallback)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(lib, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(int(stream.cuda_stream))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(fn, rc):
+    if rc != 0:
+        msg = load().kvp_last_error().decode(errors="replace")
+        raise KvpError(fn, rc, msg)
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _dtype(t):
+    if t.dtype not in _DTYPE:
+        raise ValueError(f"unsupported dtype {t.dtype}")
+    return _DTYPE[t.dtype]
+
+
+def _bhsd(q, k):
+    """Accept [B,H,S,D] or [H,S,D] (B = 1)."""
+    if q.dim() == 3:
+        q, k = q.unsqueeze(0), k.unsqueeze(0)
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q/k must be [B,H,S,D] or [H,S,D]")
+    return q, k
+
+
+def kvp_lse_pass(q, k, sm_scale=None, lse=None, stream=None):
+    """Causal row LSE: q [B,H_q,S,D], k [B,H_kv,S,D] -> lse fp32 [B,H_q,S]."""
+    squeeze = q.dim() == 3
+    q4, k4 = _bhsd(q, k)
+    B, Hq, S, D = q4.shape
+    Hkv = k4.shape[1]
+    _need(q4, "q")
+    _need(k4, "k", dtype=q4.dtype, shape=(B, Hkv, S, D))
+    if sm_scale is None:
+        sm_scale = D ** -0.5
+    if lse is None:
+        lse = torch.empty(B, Hq, S, device=q.device, dtype=torch.float32)
+    _need(lse, "lse", torch.float32)
+    if lse.numel() != B * Hq * S:
+        raise ValueError("lse has the wrong size")
+    rc = load().kvp_lse_pass(_ptr(q4), _ptr(k4), _dtype(q4), B, Hq, Hkv, S, D, float(sm_scale),
+                             _ptr(lse), _stream(stream))
+    _check("kvp_lse_pass", rc)
+    return lse[0] if squeeze and lse.dim() == 3 else lse
+
+
+def kvp_future_attn_mass_workspace_size(dtype, n_batch, h_q, h_kv, seq_len, head_dim, window):
+    dt = _DTYPE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return int(load().kvp_future_attn_mass_workspace_size(dt, n_batch, h_q, h_kv, seq_len,
+                                                          head_dim, window))
+
+
+def kvp_future_attn_mass(q, k, lse, window, sm_scale=None, F=None, workspace=None, stream=None):
+    """Future-attention mass: -> F fp32 [B,H_kv,S] (raw group sum over queries i >= j + window)."""
+    squeeze = q.dim() == 3
+    q4, k4 = _bhsd(q, k)
+    B, Hq, S, D = q4.shape
+    Hkv = k4.shape[1]
+    _need(q4, "q")
+    _need(k4, "k", dtype=q4.dtype, shape=(B, Hkv, S, D))
+    _need(lse, "lse", torch.float32)
+    if lse.numel() != B * Hq * S:
+        raise ValueError("lse has the wrong size")
+    if sm_scale is None:
+        sm_scale = D ** -0.5
+    if F is None:
+        F = torch.empty(B, Hkv, S, device=q.device, dtype=torch.float32)
+    _need(F, "F", torch.float32)
+    if F.numel() != B * Hkv * S:
+        raise ValueError("F has the wrong size")
+    need = kvp_future_attn_mass_workspace_size(q4.dtype, B, Hq, Hkv, S, D, int(window))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().kvp_future_attn_mass(_ptr(q4), _ptr(k4), _ptr(lse), _dtype(q4), B, Hq, Hkv, S, D,
+                                     float(sm_scale), int(window), _ptr(F), _ptr(workspace),
+                                     ws_bytes, _stream(stream))
+    _check("kvp_future_attn_mass", rc)
+    return F[0] if squeeze and F.dim() == 3 else F
+
+
+def kvp_soft_topk_budgets(scores, k, t, ratios=None, budgets=None, stream=None):
+    """Closed-form Soft-TopK ratios (fp64 [n]) and budgets floor(r*t) (int32 [n])."""
+    _need(scores, "scores", torch.float64)
+    n = scores.numel()
+    if ratios is None:
+        ratios = torch.empty(n, device=scores.device, dtype=torch.float64)
+    if budgets is None:
+        budgets = torch.empty(n, device=scores.device, dtype=torch.int32)
+    _need(ratios, "ratios", torch.float64, (n,))
+    _need(budgets, "budgets", torch.int32, (n,))
+    rc = load().kvp_soft_topk_budgets(_ptr(scores), n, float(k), int(t), _ptr(ratios), _ptr(budgets),
+                                      _stream(stream))
+    _check("kvp_soft_topk_budgets", rc)
+    return ratios, budgets
+
+
+def kvp_select_topk(scores, budgets, n_sink, n_recent, b_max, T=None, idx=None, count=None,
+                    stream=None):
+    """scores fp32 [R, >=T] (row stride = scores.shape[1]) -> (idx int32 [R,b_max], count int32 [R])."""
+    if scores.dim() != 2:
+        raise ValueError("scores must be [R, T]")
+    if not scores.is_cuda or scores.stride(1) != 1 or scores.dtype != torch.float32:
+        raise ValueError("scores must be a CUDA fp32 tensor with unit column stride")
+    R = scores.shape[0]
+    T = scores.shape[1] if T is None else int(T)
+    _need(budgets, "budgets", torch.int32, (R,))
+    if idx is None:
+        idx = torch.empty(R, b_max, device=scores.device, dtype=torch.int32)
+    if count is None:
+        count = torch.empty(R, device=scores.device, dtype=torch.int32)
+    _need(idx, "idx", torch.int32, (R, b_max))
+    _need(count, "count", torch.int32, (R,))
+    rc = load().kvp_select_topk(_ptr(scores), R, T, scores.stride(0), _ptr(budgets), int(n_sink),
+                                int(n_recent), _ptr(idx), int(b_max), _ptr(count), _stream(stream))
+    _check("kvp_select_topk", rc)
+    return idx, count
+
+
+def kvp_compact_kv(k, v, idx, count, k_out=None, v_out=None, stream=None):
+    """k, v [R,T,D] -> k_out, v_out [R,b_max,D] (rows m >= count[r] untouched)."""
+    _need(k, "k")
+    R, T, D = k.shape
+    _need(v, "v", k.dtype, (R, T, D))
+    b_max = idx.shape[1]
+    _need(idx, "idx", torch.int32, (R, b_max))
+    _need(count, "count", torch.int32, (R,))
+    if k_out is None:
+        k_out = torch.zeros(R, b_max, D, device=k.device, dtype=k.dtype)
+    if v_out is None:
+        v_out = torch.zeros(R, b_max, D, device=k.device, dtype=k.dtype)
+    _need(k_out, "k_out", k.dtype, (R, b_max, D))
+    _need(v_out, "v_out", k.dtype, (R, b_max, D))
+    rc = load().kvp_compact_kv(_ptr(k), _ptr(v), _dtype(k), R, T, D, _ptr(idx), _ptr(count), b_max,
+                               _ptr(k_out), _ptr(v_out), _stream(stream))
+    _check("kvp_compact_kv", rc)
+    return k_out, v_out
+
+
+def kvp_decode_attn_workspace_size(n_layers, h_q, h_kv, head_dim, T_cap, with_key_mass):
+    return int(load().kvp_decode_attn_workspace_size(n_layers, h_q, h_kv, head_dim, T_cap,
+                                                     int(bool(with_key_mass))))
+
+
+def kvp_decode_attn(q, kc, vc, lens, sm_scale=None, out=None, key_mass=None, key_pos=None,
+                    T_src=None, accumulate=False, workspace=None, stream=None):
+    """q [L,H_q,D]; kc, vc [L*H_kv,T_cap,D]; lens int32 [L*H_kv] -> out fp32 [L,H_q,D]."""
+    _need(q, "q")
+    L, Hq, D = q.shape
+    R, T_cap, _ = kc.shape
+    if R % L:
+        raise ValueError("kc rows must be n_layers * h_kv")
+    Hkv = R // L
+    _need(kc, "kc", q.dtype, (R, T_cap, D))
+    _need(vc, "vc", q.dtype, (R, T_cap, D))
+    _need(lens, "lens", torch.int32, (R,))
+    if sm_scale is None:
+        sm_scale = D ** -0.5
+    if out is None:
+        out = torch.empty(L, Hq, D, device=q.device, dtype=torch.float32)
+    _need(out, "out", torch.float32, (L, Hq, D))
+    if key_mass is not None:
+        _need(key_mass, "key_mass", torch.float32)
+        T_src = key_mass.shape[1] if T_src is None else int(T_src)
+        if key_pos is not None:
+            _need(key_pos, "key_pos", torch.int32, (R, T_cap))
+    need = kvp_decode_attn_workspace_size(L, Hq, Hkv, D, T_cap, key_mass is not None)
+    if workspace is None:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    rc = load().kvp_decode_attn(_ptr(q), _ptr(kc), _ptr(vc), _dtype(q), L, Hq, Hkv, D, T_cap,
+                                _ptr(lens), float(sm_scale), _ptr(out), _ptr(key_mass),
+                                _ptr(key_pos), int(T_src or 0), int(bool(accumulate)),
+                                _ptr(workspace), ws_bytes, _stream(stream))
+    _check("kvp_decode_attn", rc)
+    return out
+
+
+def kvp_check_device_status(stream=None):
+    rc = load().kvp_check_device_status(_stream(stream))
+    _check("kvp_check_device_status", rc)
+
+
+def kvp_abi_version():
+    return int(load().kvp_abi_version())
+
+
+def kvp_launch_count():
+    return int(load().kvp_launch_count())

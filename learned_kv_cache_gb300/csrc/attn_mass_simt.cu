@@ -1,0 +1,234 @@
+// fp32-FFMA tiled row-LSE and future-attention-mass passes.
+//
+// This is the path for float32 inputs (and a dtype-generic fallback); the
+// bf16/f16 path runs on the tensor cores (attn_mass_tc.cu).  Both passes use
+// the same 64 x 64 register-tiled score block: 256 threads, each owning a
+// 4 x 4 patch, operands staged transposed (feature-major) in shared memory so
+// that every thread reads contiguous float4s.
+//
+//  * Row pass (KVpop, "Delayed Memory Scoring", LSE example): rows = queries,
+//    columns = keys 0..i; online max / sum in base 2, one cross-lane max
+//    reduction per key tile, one sum reduction at the end.
+//  * Column pass (KVpop, Figure 2 "transposed attention"): rows = keys,
+//    columns = queries i >= j + w of every query head of the group; each
+//    thread accumulates exp2(s*log2e*scale - lse_i*log2e) of its patch rows,
+//    reduced across the 16 threads of a row at the end.
+#include "kvp_common.cuh"
+#include "kvp_launch.h"
+
+namespace kvp {
+namespace {
+
+constexpr int TM = 64;       // rows per block
+constexpr int TN = 64;       // columns per tile
+constexpr int LD = TM + 4;   // padded leading dimension of the transposed tiles
+
+// Copy rows [r0, r0 + 64) of a [S, D] matrix into sm[d * LD + r] as fp32 (zeros past S).
+template <typename T, int D>
+__device__ __forceinline__ void load_tile_t(float* sm, const T* __restrict__ src, int r0, int S) {
+  constexpr int V = Vec16<T>::N;   // elements per 16-byte vector
+  constexpr int VPR = D / V;       // vectors per row
+  for (int e = threadIdx.x; e < TM * VPR; e += blockDim.x) {
+    const int r = e / VPR, c = (e % VPR) * V;
+    float f[V];
+    if (r0 + r < S) {
+      const uint4 u = *reinterpret_cast<const uint4*>(src + (size_t)(r0 + r) * D + c);
+      Vec16<T>::unpack(u, f);
+    } else {
+#pragma unroll
+      for (int t = 0; t < V; ++t) f[t] = 0.f;
+    }
+#pragma unroll
+    for (int t = 0; t < V; ++t) sm[(c + t) * LD + r] = f[t];
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void tile_dot(const float* As, const float* Bs, int ty, int tx,
+                                         float acc[4][4]) {
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+#pragma unroll 8
+  for (int d = 0; d < D; ++d) {
+    const float4 x = *reinterpret_cast<const float4*>(As + d * LD + ty * 4);
+    const float4 y = *reinterpret_cast<const float4*>(Bs + d * LD + tx * 4);
+    const float xa[4] = {x.x, x.y, x.z, x.w};
+    const float yb[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(xa[a], yb[b], acc[a][b]);
+  }
+}
+
+__device__ __forceinline__ float row_max16(float v) {
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float row_sum16(float v) {
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256) lse_simt_kernel(const T* __restrict__ q,
+                                                       const T* __restrict__ k, int Hq, int Hkv,
+                                                       int S, float c2, float* __restrict__ lse) {
+  extern __shared__ float sm[];
+  float* As = sm;
+  float* Bs = sm + D * LD;
+  const int i0 = blockIdx.x * TM, hq = blockIdx.y, b = blockIdx.z;
+  const int G = Hq / Hkv;
+  const T* qh = q + (size_t)(b * Hq + hq) * S * D;
+  const T* kh = k + (size_t)(b * Hkv + hq / G) * S * D;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  load_tile_t<T, D>(As, qh, i0, S);
+  float m[4], l[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) { m[a] = -INFINITY; l[a] = 0.f; }
+  const int last = min(S, i0 + TM) - 1;
+  for (int j0 = 0; j0 <= last; j0 += TN) {
+    __syncthreads();
+    load_tile_t<T, D>(Bs, kh, j0, S);
+    __syncthreads();
+    float acc[4][4];
+    tile_dot<D>(As, Bs, ty, tx, acc);
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const int i = i0 + ty * 4 + a;
+      float s2[4], tmax = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int j = j0 + tx * 4 + c;
+        s2[c] = (j <= i && j < S) ? acc[a][c] * c2 : -INFINITY;
+        tmax = fmaxf(tmax, s2[c]);
+      }
+      tmax = row_max16(tmax);
+      const float mn = fmaxf(m[a], tmax);
+      if (mn == -INFINITY) continue;   // padding row past S: nothing visible
+      float add = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) add += exp2f(s2[c] - mn);
+      l[a] = l[a] * exp2f(m[a] - mn) + add;
+      m[a] = mn;
+    }
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const float tot = row_sum16(l[a]);
+    const int i = i0 + ty * 4 + a;
+    if (tx == 0 && i < S) lse[(size_t)(b * Hq + hq) * S + i] = (m[a] + log2f(tot)) * KVP_LN2;
+  }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256) fam_simt_kernel(const T* __restrict__ q,
+                                                       const T* __restrict__ k,
+                                                       const float* __restrict__ lse, int Hq,
+                                                       int Hkv, int S, float c2, int w,
+                                                       float* __restrict__ F) {
+  extern __shared__ float sm[];
+  float* As = sm;
+  float* Bs = sm + D * LD;
+  float* Ls = sm + 2 * D * LD;   // lse * log2(e) of the current query tile (+inf past S)
+  const int j0 = blockIdx.x * TM, hk = blockIdx.y, b = blockIdx.z;
+  const int G = Hq / Hkv;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float f[4] = {0.f, 0.f, 0.f, 0.f};
+  const int first = j0 + w;   // first query any key of this block receives
+  if (first < S) {
+    load_tile_t<T, D>(As, k + (size_t)(b * Hkv + hk) * S * D, j0, S);
+    for (int g = 0; g < G; ++g) {
+      const int hq = hk * G + g;
+      const T* qh = q + (size_t)(b * Hq + hq) * S * D;
+      const float* lh = lse + (size_t)(b * Hq + hq) * S;
+      for (int i0 = first; i0 < S; i0 += TN) {
+        __syncthreads();
+        load_tile_t<T, D>(Bs, qh, i0, S);
+        if (threadIdx.x < TN) {
+          const int i = i0 + threadIdx.x;
+          Ls[threadIdx.x] = i < S ? lh[i] * KVP_LOG2E : INFINITY;
+        }
+        __syncthreads();
+        float acc[4][4];
+        tile_dot<D>(As, Bs, ty, tx, acc);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const int j = j0 + ty * 4 + a;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int i = i0 + tx * 4 + c;
+            const float p = exp2f(acc[a][c] * c2 - Ls[tx * 4 + c]);
+            f[a] += (i >= j + w) ? p : 0.f;
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const float tot = row_sum16(f[a]);
+    const int j = j0 + ty * 4 + a;
+    if (tx == 0 && j < S) F[(size_t)(b * Hkv + hk) * S + j] = tot;
+  }
+}
+
+template <typename T, int D>
+cudaError_t lse_simt(const void* q, const void* k, AttnShape s, float scale, float* lse,
+                     cudaStream_t st) {
+  const size_t smem = 2 * D * LD * sizeof(float);
+  auto kern = lse_simt_kernel<T, D>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  dim3 grid((s.seq_len + TM - 1) / TM, s.h_q, s.n_batch);
+  count_launches(1);
+  kern<<<grid, 256, smem, st>>>((const T*)q, (const T*)k, s.h_q, s.h_kv, s.seq_len,
+                                scale * KVP_LOG2E, lse);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t fam_simt(const void* q, const void* k, const float* lse, AttnShape s, float scale,
+                     int w, float* F, cudaStream_t st) {
+  const size_t smem = (2 * D * LD + TN) * sizeof(float);
+  auto kern = fam_simt_kernel<T, D>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  dim3 grid((s.seq_len + TM - 1) / TM, s.h_kv, s.n_batch);
+  count_launches(1);
+  kern<<<grid, 256, smem, st>>>((const T*)q, (const T*)k, lse, s.h_q, s.h_kv, s.seq_len,
+                                scale * KVP_LOG2E, w, F);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_lse_simt(const void* q, const void* k, int dtype, AttnShape s, float scale,
+                            float* lse, cudaStream_t st) {
+  const bool d128 = s.head_dim == 128;
+  switch (dtype) {
+    case KVP_F32: return d128 ? lse_simt<float, 128>(q, k, s, scale, lse, st)
+                              : lse_simt<float, 64>(q, k, s, scale, lse, st);
+    case KVP_BF16: return d128 ? lse_simt<__nv_bfloat16, 128>(q, k, s, scale, lse, st)
+                               : lse_simt<__nv_bfloat16, 64>(q, k, s, scale, lse, st);
+    default: return d128 ? lse_simt<__half, 128>(q, k, s, scale, lse, st)
+                         : lse_simt<__half, 64>(q, k, s, scale, lse, st);
+  }
+}
+
+cudaError_t launch_fam_simt(const void* q, const void* k, const float* lse, int dtype, AttnShape s,
+                            float scale, int w, float* F, cudaStream_t st) {
+  const bool d128 = s.head_dim == 128;
+  switch (dtype) {
+    case KVP_F32: return d128 ? fam_simt<float, 128>(q, k, lse, s, scale, w, F, st)
+                              : fam_simt<float, 64>(q, k, lse, s, scale, w, F, st);
+    case KVP_BF16: return d128 ? fam_simt<__nv_bfloat16, 128>(q, k, lse, s, scale, w, F, st)
+                               : fam_simt<__nv_bfloat16, 64>(q, k, lse, s, scale, w, F, st);
+    default: return d128 ? fam_simt<__half, 128>(q, k, lse, s, scale, w, F, st)
+                         : fam_simt<__half, 64>(q, k, lse, s, scale, w, F, st);
+  }
+}
+
+}  // namespace kvp

@@ -1,0 +1,278 @@
+// C ABI of libkvp: argument validation, dispatch to the kernels, status words.
+//
+// Every entry point validates its arguments on the host and returns an error
+// before anything is enqueued; launches are asynchronous on the caller's
+// stream; the library owns no memory except one int per device (the status
+// word that kernels use to report device-side range errors and bounded-wait
+// timeouts).
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <atomic>
+#include <mutex>
+#include <string>
+
+#include "../../include/kvp.h"
+#include "kvp_launch.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+__device__ int g_device_status;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_status_mu;
+int* g_status_ptr[kMaxDevices] = {nullptr};
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+  return fail(KVP_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// Device address of this device's status word (looked up once per device).
+int status_ptr(int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(KVP_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_status);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+    g_status_ptr[dev] = (int*)p;
+  }
+  *out = g_status_ptr[dev];
+  return KVP_OK;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int elem_size(int dtype) { return dtype == KVP_F32 ? 4 : 2; }
+
+int check_dtype(int dtype) {
+  if (dtype != KVP_F32 && dtype != KVP_BF16 && dtype != KVP_F16)
+    return fail(KVP_ERR_UNSUPPORTED, "dtype %d is not one of KVP_F32/KVP_BF16/KVP_F16", dtype);
+  return KVP_OK;
+}
+
+int check_attn_shape(int n_batch, int h_q, int h_kv, int S, int D) {
+  if (n_batch < 1 || h_q < 1 || h_kv < 1 || S < 1)
+    return fail(KVP_ERR_INVALID_ARG, "n_batch=%d h_q=%d h_kv=%d seq_len=%d must be >= 1", n_batch,
+                h_q, h_kv, S);
+  if (h_q % h_kv != 0) return fail(KVP_ERR_INVALID_ARG, "h_q=%d not a multiple of h_kv=%d", h_q, h_kv);
+  if (D != 64 && D != 128) return fail(KVP_ERR_UNSUPPORTED, "head_dim=%d (64 or 128 supported)", D);
+  if ((long long)n_batch * h_q * S > (1LL << 40))
+    return fail(KVP_ERR_INVALID_ARG, "problem too large");
+  return KVP_OK;
+}
+
+std::atomic<unsigned long long> g_launches{0};
+
+#define KVP_TRY(x)            \
+  do {                        \
+    int _rc = (x);            \
+    if (_rc != KVP_OK) return _rc; \
+  } while (0)
+
+}  // namespace
+
+namespace kvp {
+void count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+}  // namespace kvp
+
+extern "C" {
+
+uint64_t kvp_launch_count(void) { return (uint64_t)g_launches.load(std::memory_order_relaxed); }
+
+int kvp_abi_version(void) { return KVP_ABI_VERSION; }
+
+const char* kvp_last_error(void) { return g_last_error.c_str(); }
+
+const char* kvp_status_string(int status) {
+  switch (status) {
+    case KVP_OK: return "ok";
+    case KVP_ERR_INVALID_ARG: return "invalid argument";
+    case KVP_ERR_UNSUPPORTED: return "unsupported dtype, head_dim or layout";
+    case KVP_ERR_CUDA: return "CUDA error";
+    case KVP_ERR_TIMEOUT: return "bounded device wait timed out";
+    case KVP_ERR_WORKSPACE: return "workspace missing or too small";
+    case KVP_ERR_DEVICE_CHECK: return "device-side range check failed";
+    default: return "unknown status";
+  }
+}
+
+int kvp_check_device_status(kvp_stream_t stream) {
+  int* st = nullptr;
+  KVP_TRY(status_ptr(&st));
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyFromSymbol(status)");
+  const int zero = 0;
+  e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyToSymbol(status)");
+  if (v != KVP_OK) return fail(v, "device status: %s", kvp_status_string(v));
+  return KVP_OK;
+}
+
+int kvp_lse_pass(const void* q, const void* k, int dtype, int n_batch, int h_q, int h_kv,
+                 int seq_len, int head_dim, float sm_scale, float* lse, kvp_stream_t stream) {
+  g_last_error.clear();
+  KVP_TRY(check_dtype(dtype));
+  KVP_TRY(check_attn_shape(n_batch, h_q, h_kv, seq_len, head_dim));
+  if (!q || !k || !lse) return fail(KVP_ERR_INVALID_ARG, "null q/k/lse");
+  if (!aligned16(q) || !aligned16(k)) return fail(KVP_ERR_INVALID_ARG, "q/k not 16-byte aligned");
+  if (!std::isfinite(sm_scale)) return fail(KVP_ERR_INVALID_ARG, "sm_scale not finite");
+  int* st = nullptr;
+  KVP_TRY(status_ptr(&st));
+  kvp::AttnShape s{n_batch, h_q, h_kv, seq_len, head_dim};
+  cudaError_t e = kvp::tc_supported(dtype, s)
+                      ? kvp::launch_lse_tc(q, k, dtype, s, sm_scale, lse, st, (cudaStream_t)stream)
+                      : kvp::launch_lse_simt(q, k, dtype, s, sm_scale, lse, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kvp_lse_pass launch");
+  return KVP_OK;
+}
+
+size_t kvp_future_attn_mass_workspace_size(int dtype, int n_batch, int h_q, int h_kv, int seq_len,
+                                           int head_dim, int window) {
+  if (check_dtype(dtype) != KVP_OK || check_attn_shape(n_batch, h_q, h_kv, seq_len, head_dim) != KVP_OK ||
+      window < 0)
+    return 0;
+  kvp::AttnShape s{n_batch, h_q, h_kv, seq_len, head_dim};
+  return kvp::tc_supported(dtype, s) ? kvp::fam_tc_workspace_size(s, window) : 0;
+}
+
+int kvp_future_attn_mass(const void* q, const void* k, const float* lse, int dtype, int n_batch,
+                         int h_q, int h_kv, int seq_len, int head_dim, float sm_scale, int window,
+                         float* F, void* workspace, size_t workspace_bytes, kvp_stream_t stream) {
+  g_last_error.clear();
+  KVP_TRY(check_dtype(dtype));
+  KVP_TRY(check_attn_shape(n_batch, h_q, h_kv, seq_len, head_dim));
+  if (!q || !k || !lse || !F) return fail(KVP_ERR_INVALID_ARG, "null q/k/lse/F");
+  if (!aligned16(q) || !aligned16(k)) return fail(KVP_ERR_INVALID_ARG, "q/k not 16-byte aligned");
+  if (window < 0) return fail(KVP_ERR_INVALID_ARG, "window=%d < 0", window);
+  if (!std::isfinite(sm_scale)) return fail(KVP_ERR_INVALID_ARG, "sm_scale not finite");
+  kvp::AttnShape s{n_batch, h_q, h_kv, seq_len, head_dim};
+  const size_t need = kvp_future_attn_mass_workspace_size(dtype, n_batch, h_q, h_kv, seq_len,
+                                                          head_dim, window);
+  if (need > 0 && (!workspace || workspace_bytes < need))
+    return fail(KVP_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+  int* st = nullptr;
+  KVP_TRY(status_ptr(&st));
+  cudaError_t e = kvp::tc_supported(dtype, s)
+                      ? kvp::launch_fam_tc(q, k, lse, dtype, s, sm_scale, window, F, workspace,
+                                           workspace_bytes, st, (cudaStream_t)stream)
+                      : kvp::launch_fam_simt(q, k, lse, dtype, s, sm_scale, window, F,
+                                             (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kvp_future_attn_mass launch");
+  return KVP_OK;
+}
+
+int kvp_soft_topk_budgets(const double* scores, int n, double k, int t, double* ratios,
+                          int32_t* budgets, kvp_stream_t stream) {
+  g_last_error.clear();
+  if (!scores || !ratios || !budgets) return fail(KVP_ERR_INVALID_ARG, "null scores/ratios/budgets");
+  if (n < 1 || n > 1024) return fail(KVP_ERR_INVALID_ARG, "n=%d outside [1, 1024]", n);
+  if (!(k > 0.0 && k < (double)n)) return fail(KVP_ERR_INVALID_ARG, "k=%g outside (0, n)", k);
+  if (t < 0) return fail(KVP_ERR_INVALID_ARG, "t=%d < 0", t);
+  cudaError_t e = kvp::launch_soft_topk(scores, n, k, t, ratios, budgets, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kvp_soft_topk_budgets launch");
+  return KVP_OK;
+}
+
+int kvp_select_topk(const float* scores, int R, int T, int64_t row_stride, const int32_t* budgets,
+                    int n_sink, int n_recent, int32_t* idx, int b_max, int32_t* count,
+                    kvp_stream_t stream) {
+  g_last_error.clear();
+  if (!scores || !budgets || !idx || !count) return fail(KVP_ERR_INVALID_ARG, "null pointer");
+  if (R < 1 || T < 1) return fail(KVP_ERR_INVALID_ARG, "R=%d T=%d must be >= 1", R, T);
+  if (row_stride < T) return fail(KVP_ERR_INVALID_ARG, "row_stride=%lld < T=%d", (long long)row_stride, T);
+  if (n_sink < 0 || n_recent < 0) return fail(KVP_ERR_INVALID_ARG, "negative n_sink/n_recent");
+  if (b_max < 1) return fail(KVP_ERR_INVALID_ARG, "b_max=%d must be >= 1", b_max);
+  if (R > 2147483647 / 2) return fail(KVP_ERR_INVALID_ARG, "R too large");
+  int* st = nullptr;
+  KVP_TRY(status_ptr(&st));
+  cudaError_t e = kvp::launch_select(scores, R, T, row_stride, budgets, n_sink, n_recent, idx, b_max,
+                                     count, st, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kvp_select_topk launch");
+  return KVP_OK;
+}
+
+int kvp_compact_kv(const void* k, const void* v, int dtype, int R, int T, int head_dim,
+                   const int32_t* idx, const int32_t* count, int b_max, void* k_out, void* v_out,
+                   kvp_stream_t stream) {
+  g_last_error.clear();
+  KVP_TRY(check_dtype(dtype));
+  if (!k || !v || !idx || !count || !k_out || !v_out) return fail(KVP_ERR_INVALID_ARG, "null pointer");
+  if (R < 1 || T < 1 || b_max < 1) return fail(KVP_ERR_INVALID_ARG, "R=%d T=%d b_max=%d must be >= 1", R, T, b_max);
+  if (head_dim != 64 && head_dim != 128) return fail(KVP_ERR_UNSUPPORTED, "head_dim=%d", head_dim);
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_out) || !aligned16(v_out))
+    return fail(KVP_ERR_INVALID_ARG, "k/v/k_out/v_out not 16-byte aligned");
+  int* st = nullptr;
+  KVP_TRY(status_ptr(&st));
+  cudaError_t e = kvp::launch_compact(k, v, head_dim * elem_size(dtype), R, T, idx, count, b_max,
+                                      k_out, v_out, st, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kvp_compact_kv launch");
+  return KVP_OK;
+}
+
+size_t kvp_decode_attn_workspace_size(int n_layers, int h_q, int h_kv, int head_dim, int T_cap,
+                                      int with_key_mass) {
+  if (n_layers < 1 || h_q < 1 || h_kv < 1 || h_q % h_kv || T_cap < 1 ||
+      (head_dim != 64 && head_dim != 128))
+    return 0;
+  return kvp::decode_plan(n_layers, h_q, h_kv, head_dim, T_cap, with_key_mass).total_bytes;
+}
+
+int kvp_decode_attn(const void* q, const void* kc, const void* vc, int dtype, int n_layers, int h_q,
+                    int h_kv, int head_dim, int T_cap, const int32_t* len, float sm_scale,
+                    float* out, float* key_mass, const int32_t* key_pos, int T_src, int accumulate,
+                    void* workspace, size_t workspace_bytes, kvp_stream_t stream) {
+  g_last_error.clear();
+  KVP_TRY(check_dtype(dtype));
+  if (!q || !kc || !vc || !len || !out) return fail(KVP_ERR_INVALID_ARG, "null q/kc/vc/len/out");
+  if (n_layers < 1 || h_q < 1 || h_kv < 1 || T_cap < 1)
+    return fail(KVP_ERR_INVALID_ARG, "n_layers=%d h_q=%d h_kv=%d T_cap=%d must be >= 1", n_layers,
+                h_q, h_kv, T_cap);
+  if (h_q % h_kv) return fail(KVP_ERR_INVALID_ARG, "h_q=%d not a multiple of h_kv=%d", h_q, h_kv);
+  if (h_q / h_kv > 8) return fail(KVP_ERR_UNSUPPORTED, "group size %d > 8", h_q / h_kv);
+  if (head_dim != 64 && head_dim != 128) return fail(KVP_ERR_UNSUPPORTED, "head_dim=%d", head_dim);
+  if (!aligned16(q) || !aligned16(kc) || !aligned16(vc))
+    return fail(KVP_ERR_INVALID_ARG, "q/kc/vc not 16-byte aligned");
+  if (!std::isfinite(sm_scale)) return fail(KVP_ERR_INVALID_ARG, "sm_scale not finite");
+  if (key_mass) {
+    if (T_src < 1) return fail(KVP_ERR_INVALID_ARG, "T_src=%d must be >= 1", T_src);
+    if (!key_pos && T_src < T_cap)
+      return fail(KVP_ERR_INVALID_ARG, "T_src=%d < T_cap=%d without key_pos", T_src, T_cap);
+    if (accumulate != 0 && accumulate != 1) return fail(KVP_ERR_INVALID_ARG, "accumulate must be 0 or 1");
+  }
+  const kvp::DecodePlan plan = kvp::decode_plan(n_layers, h_q, h_kv, head_dim, T_cap, key_mass != nullptr);
+  if (!workspace || workspace_bytes < plan.total_bytes)
+    return fail(KVP_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", plan.total_bytes,
+                workspace_bytes);
+  if (((uintptr_t)workspace & 255u) != 0) return fail(KVP_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+  int* st = nullptr;
+  KVP_TRY(status_ptr(&st));
+  cudaError_t e = kvp::launch_decode(q, kc, vc, dtype, n_layers, h_q, h_kv, head_dim, T_cap, len,
+                                     sm_scale, out, key_mass, key_pos, T_src, accumulate, plan,
+                                     workspace, st, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kvp_decode_attn launch");
+  return KVP_OK;
+}
+
+}  // extern "C"

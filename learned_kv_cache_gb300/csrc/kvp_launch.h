@@ -1,0 +1,53 @@
+// Host-side launchers of libkvp's kernels (one translation unit each); called
+// by kvp_abi.cu after argument validation.  Each returns cudaGetLastError().
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kvp {
+
+// Host-side count of kernel launches made by the library (diagnostics).
+void count_launches(int n);
+
+struct AttnShape {
+  int n_batch, h_q, h_kv, seq_len, head_dim;
+};
+
+// fp32-FFMA tiled passes (any dtype; the only path for float32 inputs).
+cudaError_t launch_lse_simt(const void* q, const void* k, int dtype, AttnShape s, float scale,
+                            float* lse, cudaStream_t st);
+cudaError_t launch_fam_simt(const void* q, const void* k, const float* lse, int dtype, AttnShape s,
+                            float scale, int window, float* F, cudaStream_t st);
+
+// tcgen05 / TMA passes (bf16 / f16, head_dim 128).
+bool tc_supported(int dtype, AttnShape s);
+size_t fam_tc_workspace_size(AttnShape s, int window);
+cudaError_t launch_lse_tc(const void* q, const void* k, int dtype, AttnShape s, float scale,
+                          float* lse, int* status, cudaStream_t st);
+cudaError_t launch_fam_tc(const void* q, const void* k, const float* lse, int dtype, AttnShape s,
+                          float scale, int window, float* F, void* ws, size_t ws_bytes,
+                          int* status, cudaStream_t st);
+
+cudaError_t launch_soft_topk(const double* x, int n, double k, int t, double* ratios,
+                             int32_t* budgets, cudaStream_t st);
+cudaError_t launch_select(const float* scores, int R, int T, int64_t row_stride,
+                          const int32_t* budgets, int n_sink, int n_recent, int32_t* idx,
+                          int b_max, int32_t* count, int* status, cudaStream_t st);
+cudaError_t launch_compact(const void* k, const void* v, int row_bytes, int R, int T,
+                           const int32_t* idx, const int32_t* count, int b_max, void* k_out,
+                           void* v_out, int* status, cudaStream_t st);
+
+struct DecodePlan {
+  int R, G, n_chunks, chunk;
+  size_t partial_bytes, lse_bytes, logit_bytes, total_bytes;
+};
+DecodePlan decode_plan(int n_layers, int h_q, int h_kv, int head_dim, int T_cap, int with_key_mass);
+cudaError_t launch_decode(const void* q, const void* kc, const void* vc, int dtype, int n_layers,
+                          int h_q, int h_kv, int head_dim, int T_cap, const int32_t* len,
+                          float scale, float* out, float* key_mass, const int32_t* key_pos,
+                          int T_src, int accumulate, const DecodePlan& plan, void* ws,
+                          int* status, cudaStream_t st);
+
+}  // namespace kvp

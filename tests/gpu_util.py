@@ -1,0 +1,44 @@
+"""Shared helpers of the GPU parity tests: tolerances and comparisons.
+
+Tolerances:
+* F (future-attention mass): max relative error 2e-3 over entries whose
+  oracle value is > 0; entries the oracle gives exactly 0 (keys past S-1-w)
+  must be exactly 0.
+* LSE: absolute error 1e-3 (a natural-log offset error e shifts every
+  probability of the row by the factor exp(e), i.e. a relative error ~e in F,
+  so 1e-3 keeps F inside its 2e-3 budget).
+* selection indices, counts and compacted K/V: bit-exact.
+* decode output: max absolute error 2e-3; key mass: relative 2e-3 plus 1e-9.
+* Soft-TopK ratios: relative 1e-12; budgets exact unless r*t lies within
+  1e-9 of an integer (then either floor is accepted).
+"""
+import numpy as np
+import torch
+
+F_RTOL = 2e-3
+LSE_ATOL = 1e-3
+DECODE_ATOL = 2e-3
+
+
+def np64(t):
+    return t.detach().to("cpu").to(torch.float64).numpy()
+
+
+def check_F(F_gpu, F_ref, what=""):
+    F_gpu = np.asarray(F_gpu, dtype=np.float64)
+    F_ref = np.asarray(F_ref, dtype=np.float64)
+    assert F_gpu.shape == F_ref.shape, (F_gpu.shape, F_ref.shape)
+    pos = F_ref > 0
+    zero = ~pos
+    assert (F_gpu[zero] == 0).all(), f"{what}: nonzero F where the oracle is exactly 0"
+    if pos.any():
+        rel = np.abs(F_gpu[pos] - F_ref[pos]) / F_ref[pos]
+        assert rel.max() <= F_RTOL, f"{what}: F max rel err {rel.max():.3e}"
+        return float(rel.max())
+    return 0.0
+
+
+def check_lse(lse_gpu, lse_ref, what=""):
+    err = np.abs(np.asarray(lse_gpu, np.float64) - np.asarray(lse_ref, np.float64)).max()
+    assert err <= LSE_ATOL, f"{what}: lse max abs err {err:.3e}"
+    return float(err)
