@@ -1,17 +1,528 @@
-// Tensor-core (tcgen05 / TMEM / TMA) row-LSE and future-attention-mass passes.
+// Tensor-core row-LSE and future-attention-mass passes (sm_103a: tcgen05 MMA
+// with TMEM accumulators, operands staged by TMA in 128-byte-swizzled shared
+// memory).
+//
+// Both passes are the same contraction, S = A * B^T with A a fixed 128-row
+// tile of the CTA and B a stream of 128-row tiles, followed by a fused
+// per-row softmax epilogue that reads the fp32 scores straight from TMEM:
+//
+//  * row LSE (KVpop, "Delayed Memory Scoring", LSE worked example): A = a
+//    query tile, B = the key tiles 0..qt (causal); each TMEM lane is one query
+//    row; online max / sum in base 2; the diagonal tile is masked j <= i.
+//  * future-attention mass (KVpop, Figure 2, transposed attention): roles
+//    swapped, A = a key tile, B = the query tiles i >= j + w of every query
+//    head of the GQA group; each TMEM lane is one key row and simply
+//    accumulates exp2(s*log2e*scale - lse_i*log2e) over its columns, so the
+//    column sums of the attention matrix become per-thread row sums with no
+//    atomics; only the first query tile (the window diagonal) is masked
+//    i >= j + w; queries past S get lse = +inf (weight 0).
+//
+// CTA layout (320 threads, 2 CTAs per SM): warps 0-7 epilogue (warp w reads
+// TMEM lanes 32*(w%4).., columns half w/4 of each tile), warp 8 TMA producer,
+// warp 9 TMEM allocator + MMA issuer (one elected thread).  Shared memory:
+// A tile (32 KB) + 2 B stages (2 x 32 KB); TMEM: 2 accumulators of 128 fp32
+// columns so the MMA of tile t+1 overlaps the epilogue of tile t.
+//
+// Work: one CTA per work item, ordered heaviest first so the block scheduler
+// balances the triangular work.  Row-LSE items are (query head, query tile),
+// longest rows first.  Mass items are (KV head, key tile, query chunk of TPC
+// tiles): a key row is split along the query axis into chunks whose partial
+// sums go to the workspace and are added in fixed order by a reduce kernel
+// (deterministic).
+#include <cuda.h>
+
+#include <algorithm>
+#include <mutex>
+
 #include "kvp_common.cuh"
 #include "kvp_launch.h"
+#include "tc_ptx.cuh"
 
 namespace kvp {
+namespace {
 
-bool tc_supported(int, AttnShape) { return false; }
-size_t fam_tc_workspace_size(AttnShape, int) { return 0; }
-cudaError_t launch_lse_tc(const void*, const void*, int, AttnShape, float, float*, int*, cudaStream_t) {
-  return cudaErrorNotSupported;
+constexpr int BM = 128;            // rows of the fixed A tile (TMEM lanes)
+constexpr int BN = 128;            // rows of a streamed B tile (TMEM columns per accumulator)
+constexpr int HD = 128;            // head dim (MMA K)
+constexpr int NSTAGE = 2;          // B tiles in flight
+constexpr int NACC = 2;            // TMEM accumulators
+constexpr int EPI_WARPS = 8;
+constexpr int PRODUCER_WARP = 8;
+constexpr int MMA_WARP = 9;
+constexpr int THREADS = 32 * (EPI_WARPS + 2);
+constexpr int TILE_BYTES = 128 * HD * 2;         // 32 KB: two 128-row x 128-byte halves
+constexpr int HALF_BYTES = TILE_BYTES / 2;
+constexpr int TMEM_COLS = NACC * BN;             // 256
+
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + TILE_BYTES;
+constexpr int OFF_BAR = OFF_B + NSTAGE * TILE_BYTES;
+constexpr int OFF_MISC = OFF_BAR + 256;
+constexpr int OFF_NL2 = OFF_MISC + 64;
+constexpr int OFF_RED = OFF_NL2 + EPI_WARPS * 64 * 4;
+constexpr int SMEM_BYTES = OFF_RED + 2 * BM * 4 * 2 + 1024;   // + alignment slack
+
+struct TcParams {
+  int S, Hq, Hkv, G;
+  float c2;              // sm_scale * log2(e)
+  int window;
+  const float* lse;      // mass pass: natural-log row LSE [B*Hq*S]
+  float* out;            // LSE pass: lse [B*Hq*S]; mass pass: partial sums (workspace)
+  int n_groups;          // LSE pass: B*Hq; mass pass: B*Hkv
+  int NQT;               // LSE pass: query tiles per head
+  int NT0, TPC, CMAX, NKT, Nf;   // mass pass schedule
+  int* status;
+};
+
+struct Item {
+  int group;             // LSE: b*Hq+hq; mass: b*Hkv+h
+  int tile;              // LSE: query tile qt; mass: key tile jt
+  int chunk;             // mass: chunk index within the key row
+  int per_head;          // mass: query tiles per head in this item
+  int n_tiles;           // B tiles streamed by this CTA
+};
+
+template <int MODE>
+__device__ __forceinline__ Item decode_item(int I, const TcParams& p) {
+  Item it;
+  if (MODE == 0) {
+    it.group = I % p.n_groups;
+    it.tile = p.NQT - 1 - I / p.n_groups;
+    it.chunk = 0;
+    it.per_head = 0;
+    it.n_tiles = it.tile + 1;
+  } else {
+    const long long full_total = (long long)p.Nf * p.n_groups;
+    if (I < full_total) {
+      int local = I / p.n_groups;
+      it.group = I % p.n_groups;
+      int c = 0;
+      while (true) {
+        const int n_c = p.NT0 - p.TPC * (c + 1) + 1;
+        if (local < n_c) break;
+        local -= n_c;
+        ++c;
+      }
+      it.tile = local;
+      it.chunk = c;
+      it.per_head = p.TPC;
+    } else {
+      int local = (int)((I - full_total) / p.n_groups);
+      it.group = (int)((I - full_total) % p.n_groups);
+      it.tile = 0;
+      it.chunk = 0;
+      it.per_head = 0;
+      for (int r = p.TPC - 1; r >= 1; --r) {
+        const int cnt = p.NT0 >= r ? (p.NT0 - r) / p.TPC + 1 : 0;
+        if (local < cnt) {
+          it.tile = p.NT0 - r - local * p.TPC;
+          it.chunk = local;
+          it.per_head = r;
+          break;
+        }
+        local -= cnt;
+      }
+    }
+    it.n_tiles = it.per_head * p.G;
+  }
+  return it;
 }
-cudaError_t launch_fam_tc(const void*, const void*, const float*, int, AttnShape, float, int, float*,
-                          void*, size_t, int*, cudaStream_t) {
-  return cudaErrorNotSupported;
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 2)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const TcParams p, const bool bf16) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s_base = ptx::smem_u32(smem);
+  const uint32_t sA = s_base + OFF_A;
+  const uint32_t sB = s_base + OFF_B;
+  const uint32_t bar_full = s_base + OFF_BAR;                  // [NSTAGE]
+  const uint32_t bar_empty = bar_full + 8 * NSTAGE;            // [NSTAGE]
+  const uint32_t bar_accf = bar_empty + 8 * NSTAGE;            // [NACC]
+  const uint32_t bar_acce = bar_accf + 8 * NACC;               // [NACC]
+  const uint32_t bar_a = bar_acce + 8 * NACC;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+  float* nl2_all = reinterpret_cast<float*>(smem + OFF_NL2);
+  float* red = reinterpret_cast<float*>(smem + OFF_RED);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Item it = decode_item<MODE>(blockIdx.x, p);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      ptx::mbar_init(bar_full + 8 * s, 1);
+      ptx::mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int a = 0; a < NACC; ++a) {
+      ptx::mbar_init(bar_accf + 8 * a, 1);
+      ptx::mbar_init(bar_acce + 8 * a, EPI_WARPS);
+    }
+    ptx::mbar_init(bar_a, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == MMA_WARP) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_holder), TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  if (warp == PRODUCER_WARP && lane == 0) {
+    ptx::prefetch_tmap(&tmQ);
+    ptx::prefetch_tmap(&tmK);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  // Coordinates of the fixed A tile and of streamed tile t.
+  int a_row, a_z, kv_z = 0, b_of_group = 0, hkv = 0;
+  if (MODE == 0) {
+    a_row = it.tile * BM;
+    a_z = it.group;
+    b_of_group = it.group / p.Hq;
+    kv_z = b_of_group * p.Hkv + (it.group % p.Hq) / p.G;
+  } else {
+    a_row = it.tile * BM;
+    a_z = it.group;                // K tensor map z = b*Hkv + h
+    b_of_group = it.group / p.Hkv;
+    hkv = it.group % p.Hkv;
+  }
+  const int j0 = it.tile * BM;     // mass pass: first key of the tile
+  auto b_coords = [&](int t, int& row, int& z) {
+    if (MODE == 0) {
+      row = t * BN;
+      z = kv_z;
+    } else {
+      const int gh = t / it.per_head, u = t % it.per_head;
+      row = j0 + p.window + BN * (it.chunk * p.TPC + u);
+      z = b_of_group * p.Hq + hkv * p.G + gh;
+    }
+  };
+
+  if (warp == PRODUCER_WARP) {
+    if (lane == 0) {
+      const CUtensorMap* tmA = MODE == 0 ? &tmQ : &tmK;
+      const CUtensorMap* tmB = MODE == 0 ? &tmK : &tmQ;
+      ptx::mbar_arrive_expect_tx(bar_a, TILE_BYTES);
+      ptx::tma_load_3d(sA, tmA, bar_a, 0, a_row, a_z);
+      ptx::tma_load_3d(sA + HALF_BYTES, tmA, bar_a, 64, a_row, a_z);
+      int t = 0;
+      for (; t < it.n_tiles; ++t) {
+        const int s = t % NSTAGE, use = t / NSTAGE;
+        if (use > 0 && !ptx::mbar_wait(bar_empty + 8 * s, (use - 1) & 1, abort_flag, p.status)) break;
+        int row, z;
+        b_coords(t, row, z);
+        const uint32_t dst = sB + s * TILE_BYTES;
+        ptx::mbar_arrive_expect_tx(bar_full + 8 * s, TILE_BYTES);
+        ptx::tma_load_3d(dst, tmB, bar_full + 8 * s, 0, row, z);
+        ptx::tma_load_3d(dst + HALF_BYTES, tmB, bar_full + 8 * s, 64, row, z);
+      }
+      // Let every copy this thread started land before the CTA can exit.
+      ptx::mbar_wait(bar_a, 0, abort_flag, p.status);
+      for (int q = max(0, t - NSTAGE); q < t; ++q)
+        ptx::mbar_wait(bar_full + 8 * (q % NSTAGE), (q / NSTAGE) & 1, abort_flag, p.status);
+    }
+  } else if (warp == MMA_WARP) {
+    if (lane == 0) {
+      const uint32_t idesc = ptx::idesc_f16(bf16, BM, BN);
+      int t = 0;
+      if (ptx::mbar_wait(bar_a, 0, abort_flag, p.status)) {
+        for (; t < it.n_tiles; ++t) {
+          const int s = t % NSTAGE, a = t % NACC;
+          if (!ptx::mbar_wait(bar_full + 8 * s, (t / NSTAGE) & 1, abort_flag, p.status)) break;
+          if (t >= NACC && !ptx::mbar_wait(bar_acce + 8 * a, ((t / NACC) - 1) & 1, abort_flag, p.status))
+            break;
+          ptx::tc_fence_after();
+          const uint32_t d = tmem + a * BN;
+          const uint32_t bs = sB + s * TILE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
+            ptx::mma_f16_ss(d, ptx::desc_sw128(sA + off), ptx::desc_sw128(bs + off), idesc, kk > 0);
+          }
+          ptx::mma_commit(bar_empty + 8 * s);
+          ptx::mma_commit(bar_accf + 8 * a);
+        }
+      }
+      // The MMAs of the last issued tile must finish before TMEM is released.
+      if (t > 0) ptx::mbar_wait(bar_accf + 8 * ((t - 1) % NACC), ((t - 1) / NACC) & 1, abort_flag, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int half = warp >> 2, quad = warp & 3;
+    const int r = quad * 32 + lane;            // row of the A tile handled by this thread
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    float* nl2 = nl2_all + warp * 64;
+    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;   // mass pass partial sums
+    float m = -INFINITY, l = 0.f;                            // LSE pass running state
+    bool ok = true;
+    for (int t = 0; t < it.n_tiles; ++t) {
+      const int a = t % NACC;
+      if (!ptx::mbar_wait(bar_accf + 8 * a, (t / NACC) & 1, abort_flag, p.status)) { ok = false; break; }
+      ptx::tc_fence_after();
+      uint32_t v[64];
+      {
+        uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
+        uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
+        const uint32_t taddr = tmem + lane_base + a * BN + half * 64;
+        ptx::tmem_ld32(taddr, v0);
+        ptx::tmem_ld32(taddr + 32, v1);
+        ptx::tmem_ld_wait();
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar_acce + 8 * a);
+
+      if (MODE == 0) {
+        const bool diag = (t == it.tile);
+        if (diag) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (half * 64 + c > r) v[c] = __float_as_uint(-INFINITY);
+        }
+        float tm = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) tm = max3(tm, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+        const float mn = fmaxf(m, tm * p.c2);
+        if (mn == -INFINITY) continue;
+        if (mn > m) {
+          l *= fast_exp2(m - mn);
+          m = mn;
+        }
+        const float nm = -m;
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+          s0 += fast_exp2(fmaf(__uint_as_float(v[c]), p.c2, nm));
+          s1 += fast_exp2(fmaf(__uint_as_float(v[c + 1]), p.c2, nm));
+          s2 += fast_exp2(fmaf(__uint_as_float(v[c + 2]), p.c2, nm));
+          s3 += fast_exp2(fmaf(__uint_as_float(v[c + 3]), p.c2, nm));
+        }
+        l += (s0 + s1) + (s2 + s3);
+      } else {
+        const int gh = t / it.per_head, u = t % it.per_head;
+        const int i0 = j0 + p.window + BN * (it.chunk * p.TPC + u) + half * 64;
+        const float* lrow = p.lse + (size_t)(b_of_group * p.Hq + hkv * p.G + gh) * p.S;
+        {
+          const int ia = i0 + 2 * lane;
+          nl2[2 * lane] = ia < p.S ? -lrow[ia] * KVP_LOG2E : -INFINITY;
+          nl2[2 * lane + 1] = ia + 1 < p.S ? -lrow[ia + 1] * KVP_LOG2E : -INFINITY;
+        }
+        __syncwarp();
+        const bool diag = (it.chunk == 0 && u == 0);
+        if (diag) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (half * 64 + c < r) v[c] = __float_as_uint(-INFINITY);
+        }
+        const float4* n4 = reinterpret_cast<const float4*>(nl2);
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+          const float4 n = n4[c >> 2];
+          acc0 += fast_exp2(fmaf(__uint_as_float(v[c]), p.c2, n.x));
+          acc1 += fast_exp2(fmaf(__uint_as_float(v[c + 1]), p.c2, n.y));
+          acc2 += fast_exp2(fmaf(__uint_as_float(v[c + 2]), p.c2, n.z));
+          acc3 += fast_exp2(fmaf(__uint_as_float(v[c + 3]), p.c2, n.w));
+        }
+        __syncwarp();
+      }
+    }
+    // Combine the two column halves of every row and write the result.
+    asm volatile("bar.sync 1, %0;" ::"r"(EPI_WARPS * 32));
+    if (MODE == 0) {
+      if (half == 1) {
+        red[r] = m;
+        red[BM + r] = l;
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(EPI_WARPS * 32));
+      if (half == 0 && ok && !*abort_flag) {
+        const float m1 = red[r], l1 = red[BM + r];
+        const float M = fmaxf(m, m1);
+        float L = 0.f;
+        if (M != -INFINITY) L = (m == -INFINITY ? 0.f : l * fast_exp2(m - M)) +
+                                (m1 == -INFINITY ? 0.f : l1 * fast_exp2(m1 - M));
+        const int i = it.tile * BM + r;
+        if (i < p.S) p.out[(size_t)it.group * p.S + i] = (M + __log2f(L)) * KVP_LN2;
+      }
+    } else {
+      const float f = (acc0 + acc1) + (acc2 + acc3);
+      if (half == 1) red[r] = f;
+      asm volatile("bar.sync 1, %0;" ::"r"(EPI_WARPS * 32));
+      if (half == 0 && ok && !*abort_flag && it.n_tiles > 0) {
+        float* dst = p.out + ((size_t)it.group * p.NKT + it.tile) * p.CMAX * BM + (size_t)it.chunk * BM;
+        dst[r] = f + red[r];
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// F[group, j] = sum over the chunks of key tile j/128 of the partial sums, in chunk order.
+__global__ void __launch_bounds__(BM) fam_reduce_kernel(const float* __restrict__ part, int S, int NT0,
+                                                        int TPC, int CMAX, int NKT,
+                                                        float* __restrict__ F) {
+  const int jt = blockIdx.x, group = blockIdx.y, r = threadIdx.x;
+  const int j = jt * BM + r;
+  if (j >= S) return;
+  const int nt = max(0, NT0 - jt);
+  const int nch = (nt + TPC - 1) / TPC;
+  const float* src = part + ((size_t)group * NKT + jt) * CMAX * BM + r;
+  float f = 0.f;
+  for (int c = 0; c < nch; ++c) f += src[(size_t)c * BM];
+  F[(size_t)group * S + j] = f;
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// [n_heads, S, 128] tensor, 128-row x 64-element boxes, 128-byte swizzle, zero fill past S.
+bool make_tmap(CUtensorMap* m, const void* base, int dtype, int n_heads, int S) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)HD, (cuuint64_t)S, (cuuint64_t)n_heads};
+  cuuint64_t strides[2] = {(cuuint64_t)HD * 2, (cuuint64_t)S * HD * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt =
+      dtype == KVP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct FamSched {
+  int NT0, TPC, CMAX, NKT, Nf, Np;
+};
+
+FamSched fam_schedule(AttnShape s, int window) {
+  FamSched f{};
+  const int n_groups = s.n_batch * s.h_kv;
+  f.NKT = (s.seq_len + BM - 1) / BM;
+  f.NT0 = s.seq_len > window ? (s.seq_len - window + BN - 1) / BN : 0;
+  // Chunk length (query tiles per head per item): enough items for ~8 per SM.
+  const double tiles = 0.5 * (double)n_groups * f.NT0 * (f.NT0 + 1);
+  int tpc = 64;
+  while (tpc > 2 && tiles / tpc < 8.0 * 152) tpc >>= 1;
+  f.TPC = tpc;
+  f.CMAX = std::max(1, (f.NT0 + tpc - 1) / tpc);
+  f.Nf = 0;
+  for (int c = 0;; ++c) {
+    const int n_c = f.NT0 - tpc * (c + 1) + 1;
+    if (n_c <= 0) break;
+    f.Nf += n_c;
+  }
+  f.Np = 0;
+  for (int r = 1; r < tpc; ++r)
+    if (f.NT0 >= r) f.Np += (f.NT0 - r) / tpc + 1;
+  return f;
+}
+
+template <int MODE>
+cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const TcParams& p, int grid,
+                      bool bf16, cudaStream_t st) {
+  auto kern = attn_tc_kernel<MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  count_launches(1);
+  kern<<<grid, THREADS, SMEM_BYTES, st>>>(tq, tk, p, bf16);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_supported(int dtype, AttnShape s) {
+  return (dtype == KVP_BF16 || dtype == KVP_F16) && s.head_dim == HD && encode_fn() != nullptr;
+}
+
+size_t fam_tc_workspace_size(AttnShape s, int window) {
+  const FamSched f = fam_schedule(s, window);
+  return (size_t)s.n_batch * s.h_kv * f.NKT * f.CMAX * BM * sizeof(float);
+}
+
+cudaError_t launch_lse_tc(const void* q, const void* k, int dtype, AttnShape s, float scale,
+                          float* lse, int* status, cudaStream_t st) {
+  CUtensorMap tq, tk;
+  if (!make_tmap(&tq, q, dtype, s.n_batch * s.h_q, s.seq_len) ||
+      !make_tmap(&tk, k, dtype, s.n_batch * s.h_kv, s.seq_len))
+    return cudaErrorInvalidValue;
+  TcParams p{};
+  p.S = s.seq_len;
+  p.Hq = s.h_q;
+  p.Hkv = s.h_kv;
+  p.G = s.h_q / s.h_kv;
+  p.c2 = scale * KVP_LOG2E;
+  p.out = lse;
+  p.n_groups = s.n_batch * s.h_q;
+  p.NQT = (s.seq_len + BM - 1) / BM;
+  p.status = status;
+  return launch_tc<0>(tq, tk, p, p.n_groups * p.NQT, dtype == KVP_BF16, st);
+}
+
+cudaError_t launch_fam_tc(const void* q, const void* k, const float* lse, int dtype, AttnShape s,
+                          float scale, int window, float* F, void* ws, size_t ws_bytes, int* status,
+                          cudaStream_t st) {
+  const FamSched f = fam_schedule(s, window);
+  if (ws_bytes < fam_tc_workspace_size(s, window)) return cudaErrorInvalidValue;
+  TcParams p{};
+  p.S = s.seq_len;
+  p.Hq = s.h_q;
+  p.Hkv = s.h_kv;
+  p.G = s.h_q / s.h_kv;
+  p.c2 = scale * KVP_LOG2E;
+  p.window = window;
+  p.lse = lse;
+  p.out = (float*)ws;
+  p.n_groups = s.n_batch * s.h_kv;
+  p.NT0 = f.NT0;
+  p.TPC = f.TPC;
+  p.CMAX = f.CMAX;
+  p.NKT = f.NKT;
+  p.Nf = f.Nf;
+  p.status = status;
+  const long long items = (long long)(f.Nf + f.Np) * p.n_groups;
+  if (items > 0) {
+    CUtensorMap tq, tk;
+    if (!make_tmap(&tq, q, dtype, s.n_batch * s.h_q, s.seq_len) ||
+        !make_tmap(&tk, k, dtype, s.n_batch * s.h_kv, s.seq_len))
+      return cudaErrorInvalidValue;
+    if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+    cudaError_t e = launch_tc<1>(tq, tk, p, (int)items, dtype == KVP_BF16, st);
+    if (e != cudaSuccess) return e;
+  }
+  count_launches(1);
+  fam_reduce_kernel<<<dim3(f.NKT, p.n_groups), BM, 0, st>>>((const float*)ws, s.seq_len, f.NT0, f.TPC,
+                                                            f.CMAX, f.NKT, F);
+  return cudaGetLastError();
 }
 
 }  // namespace kvp

@@ -83,7 +83,7 @@ def test_uniform_attention_closed_form_on_gpu(kvp):
     check_lse(np64(lse), np.log(np.arange(1, S + 1))[None].repeat(G, 0), "uniform")
     H = np.concatenate([[0.0], np.cumsum(1.0 / np.arange(1, S + 1))])
     want = np.array([G * (H[S] - H[j + w]) if j <= S - 1 - w else 0.0 for j in range(S)])
-    check_F(np64(F[0]), want[None], "uniform")
+    check_F(np64(F), want[None], "uniform")
 
 
 def test_qwen3_4b_layer_full_size(kvp):
