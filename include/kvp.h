@@ -193,6 +193,39 @@ int kvp_decode_attn(const void* q, const void* kc, const void* vc, int dtype, in
                     kvp_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * A5 without a workspace: kvp_decode_attn_noalloc.
+ *
+ * Not a step of the method -- the pages have no counterpart.  It exists for
+ * callers that cannot hand the library a workspace: programs whose device
+ * memory is already fully reserved by their own pool (an inference server
+ * that carved HBM into its KV cache), plain-C hosts with no device allocator
+ * of their own, and decode loops that must not call cudaMalloc/cudaFree,
+ * which can synchronise the whole device and stall work on other streams.
+ *
+ * Same computation, arguments and output as kvp_decode_attn without the key
+ * mass (no key_mass / key_pos / T_src / accumulate) and without the
+ * workspace: the split-K partials go to a fixed scratch array of
+ * KVP_DECODE_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that
+ * loads the library holds until the process exits.  A shape whose partials
+ * need more than that is rejected with KVP_ERR_WORKSPACE (and a message
+ * naming both sizes) before anything is launched.  The call allocates
+ * nothing and calls no allocating routine.
+ *
+ * - The first call on each device looks up the scratch array's device
+ *   address (a CUDA runtime query, cached per device); make that first call
+ *   before capturing any stream on that device.
+ * - All calls on a device share the one array and it keeps the last call's
+ *   contents; nothing in it needs to start at zero (every partial is written
+ *   before it is read).  Calls whose executions overlap on the GPU (different
+ *   streams, or host threads without ordering) race on the scratch and
+ *   produce wrong outputs: serialise them, e.g. on one stream.
+ * ------------------------------------------------------------------------- */
+#define KVP_DECODE_NOALLOC_SCRATCH_BYTES (8u << 20) /* 8 MiB per device */
+int kvp_decode_attn_noalloc(const void* q, const void* kc, const void* vc, int dtype, int n_layers,
+                            int h_q, int h_kv, int head_dim, int T_cap, const int32_t* len,
+                            float sm_scale, float* out, kvp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Status and diagnostics.
  * ------------------------------------------------------------------------- */
 /* Static string for a kvp_status code. */

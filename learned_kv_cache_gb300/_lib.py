@@ -34,6 +34,7 @@ SIGNATURES = {
     "kvp_decode_attn_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "kvp_decode_attn": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _F, _P, _P, _P, _I, _I, _P,
                              _SZ, _P]),
+    "kvp_decode_attn_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _F, _P, _P]),
     "kvp_status_string": (ctypes.c_char_p, [_I]),
     "kvp_last_error": (ctypes.c_char_p, []),
     "kvp_check_device_status": (_I, [_P]),
@@ -260,6 +261,30 @@ def kvp_decode_attn(q, kc, vc, lens, sm_scale=None, out=None, key_mass=None, key
                                 _ptr(key_pos), int(T_src or 0), int(bool(accumulate)),
                                 _ptr(workspace), ws_bytes, _stream(stream))
     _check("kvp_decode_attn", rc)
+    return out
+
+
+def kvp_decode_attn_noalloc(q, kc, vc, lens, sm_scale=None, out=None, stream=None):
+    """kvp_decode_attn without a workspace (the library's fixed per-device scratch is used
+    instead); for callers that cannot allocate device memory.  Calls on one device must not
+    overlap on the GPU."""
+    _need(q, "q")
+    L, Hq, D = q.shape
+    R, T_cap, _ = kc.shape
+    if R % L:
+        raise ValueError("kc rows must be n_layers * h_kv")
+    _need(kc, "kc", q.dtype, (R, T_cap, D))
+    _need(vc, "vc", q.dtype, (R, T_cap, D))
+    _need(lens, "lens", torch.int32, (R,))
+    if sm_scale is None:
+        sm_scale = D ** -0.5
+    if out is None:
+        out = torch.empty(L, Hq, D, device=q.device, dtype=torch.float32)
+    _need(out, "out", torch.float32, (L, Hq, D))
+    rc = load().kvp_decode_attn_noalloc(_ptr(q), _ptr(kc), _ptr(vc), _dtype(q), L, Hq, R // L, D,
+                                        T_cap, _ptr(lens), float(sm_scale), _ptr(out),
+                                        _stream(stream))
+    _check("kvp_decode_attn_noalloc", rc)
     return out
 
 

@@ -18,11 +18,22 @@
 // each logit in the workspace and, once the row's log-sum-exp is known,
 // adds the group-summed probability of every retained key at its source
 // position.
+#include <mutex>
+
 #include "kvp_common.cuh"
 #include "kvp_launch.h"
 
 namespace kvp {
 namespace {
+
+// Scratch of kvp_decode_attn_noalloc: the split-K partials live here instead
+// of in a caller-provided workspace.  Every GPU that loads the library keeps
+// this array for the life of the process; all calls on a device share it.
+static __device__ __align__(256) unsigned char g_decode_noalloc_scratch[KVP_DECODE_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoallocMaxDevices] = {nullptr};
 
 constexpr int MAXG = 8;
 constexpr int DEC_WARPS = 4;
@@ -256,6 +267,27 @@ DecodePlan decode_plan(int n_layers, int h_q, int h_kv, int head_dim, int T_cap,
   p.logit_bytes = with_key_mass ? align256((size_t)p.R * p.G * T_cap * sizeof(float)) : 0;
   p.total_bytes = p.partial_bytes + p.lse_bytes + p.logit_bytes;
   return p;
+}
+
+// Device address of the static decode scratch on the current device.  In host
+// code the array's name only stands in for the symbol, so the address is
+// looked up with cudaGetSymbolAddress, once per device, with that device
+// current, and cached.
+cudaError_t decode_noalloc_scratch(void** ptr, size_t* bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kNoallocMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = p;
+  }
+  *ptr = g_noalloc_ptr[dev];
+  *bytes = sizeof(g_decode_noalloc_scratch);
+  return cudaSuccess;
 }
 
 cudaError_t launch_decode(const void* q, const void* kc, const void* vc, int dtype, int n_layers,

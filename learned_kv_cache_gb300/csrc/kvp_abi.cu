@@ -275,4 +275,38 @@ int kvp_decode_attn(const void* q, const void* kc, const void* vc, int dtype, in
   return KVP_OK;
 }
 
+int kvp_decode_attn_noalloc(const void* q, const void* kc, const void* vc, int dtype, int n_layers,
+                            int h_q, int h_kv, int head_dim, int T_cap, const int32_t* len,
+                            float sm_scale, float* out, kvp_stream_t stream) {
+  g_last_error.clear();
+  KVP_TRY(check_dtype(dtype));
+  if (!q || !kc || !vc || !len || !out) return fail(KVP_ERR_INVALID_ARG, "null q/kc/vc/len/out");
+  if (n_layers < 1 || h_q < 1 || h_kv < 1 || T_cap < 1)
+    return fail(KVP_ERR_INVALID_ARG, "n_layers=%d h_q=%d h_kv=%d T_cap=%d must be >= 1", n_layers,
+                h_q, h_kv, T_cap);
+  if (h_q % h_kv) return fail(KVP_ERR_INVALID_ARG, "h_q=%d not a multiple of h_kv=%d", h_q, h_kv);
+  if (h_q / h_kv > 8) return fail(KVP_ERR_UNSUPPORTED, "group size %d > 8", h_q / h_kv);
+  if (head_dim != 64 && head_dim != 128) return fail(KVP_ERR_UNSUPPORTED, "head_dim=%d", head_dim);
+  if (!aligned16(q) || !aligned16(kc) || !aligned16(vc))
+    return fail(KVP_ERR_INVALID_ARG, "q/kc/vc not 16-byte aligned");
+  if (!std::isfinite(sm_scale)) return fail(KVP_ERR_INVALID_ARG, "sm_scale not finite");
+  const kvp::DecodePlan plan = kvp::decode_plan(n_layers, h_q, h_kv, head_dim, T_cap, 0);
+  if (plan.total_bytes > (size_t)KVP_DECODE_NOALLOC_SCRATCH_BYTES)
+    return fail(KVP_ERR_WORKSPACE,
+                "this shape needs %zu bytes of scratch; the built-in scratch of "
+                "kvp_decode_attn_noalloc holds %zu (use kvp_decode_attn with a workspace)",
+                plan.total_bytes, (size_t)KVP_DECODE_NOALLOC_SCRATCH_BYTES);
+  void* scratch = nullptr;
+  size_t scratch_bytes = 0;
+  cudaError_t e = kvp::decode_noalloc_scratch(&scratch, &scratch_bytes);
+  if (e != cudaSuccess) return cuda_fail(e, "kvp_decode_attn_noalloc scratch lookup");
+  if (scratch_bytes < plan.total_bytes) return fail(KVP_ERR_WORKSPACE, "scratch smaller than plan");
+  int* st = nullptr;
+  KVP_TRY(status_ptr(&st));
+  e = kvp::launch_decode(q, kc, vc, dtype, n_layers, h_q, h_kv, head_dim, T_cap, len, sm_scale, out,
+                         nullptr, nullptr, 0, 0, plan, scratch, st, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kvp_decode_attn_noalloc launch");
+  return KVP_OK;
+}
+
 }  // extern "C"

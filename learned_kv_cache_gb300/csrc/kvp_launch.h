@@ -44,6 +44,8 @@ struct DecodePlan {
   size_t partial_bytes, lse_bytes, logit_bytes, total_bytes;
 };
 DecodePlan decode_plan(int n_layers, int h_q, int h_kv, int head_dim, int T_cap, int with_key_mass);
+// Static scratch of kvp_decode_attn_noalloc on the current device (set up on first use).
+cudaError_t decode_noalloc_scratch(void** ptr, size_t* bytes);
 cudaError_t launch_decode(const void* q, const void* kc, const void* vc, int dtype, int n_layers,
                           int h_q, int h_kv, int head_dim, int T_cap, const int32_t* len,
                           float scale, float* out, float* key_mass, const int32_t* key_pos,
