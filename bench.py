@@ -62,58 +62,80 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clock / throttle reasons during the timed region."""
+    """nvidia-smi samples of SM clock, power and throttle reasons, kept with host timestamps so
+    that only the samples taken inside the timed region are summarised."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, gpu_index):
-        self.gpu = gpu_index
-        self.proc = None
-        self.out = None
+    def __init__(self, gpu_index, period_ms=20):
+        self.gpu, self.period = gpu_index, period_ms
+        self.proc, self.rows, self.thread = None, [], None
+        self.windows = []
 
     def __enter__(self):
+        import threading
         try:
-            self.out = tempfile.TemporaryFile(mode="w+")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=self.out, stderr=subprocess.DEVNULL)
+                 "--format=csv,noheader,nounits", "-lms", str(self.period)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
-        time.sleep(0.3)
+            return self
+
+        def reader():
+            for line in self.proc.stdout:
+                self.rows.append((time.time(), line.strip()))
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+        time.sleep(0.2)
         return self
+
+    def mark(self, t0, t1):
+        self.windows.append((t0, t1))
 
     def __exit__(self, *a):
         if self.proc is not None:
+            time.sleep(0.1)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+            if self.thread is not None:
+                self.thread.join(timeout=2)
 
     def summary(self):
-        if self.proc is None or self.out is None:
+        if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.out.seek(0)
-        rows = [r for r in csv.reader(io.StringIO(self.out.read())) if len(r) >= 9]
+
+        def inside(ts, slack):
+            return any(a - slack <= ts <= b + slack for a, b in self.windows)
+        picked, how = [], "inside the timed region"
+        for slack in (0.0, 0.05, 0.2):
+            picked = [r for ts, r in self.rows if inside(ts, slack)]
+            if picked:
+                if slack:
+                    how = f"within {int(slack * 1e3)} ms of the timed region"
+                break
         sms, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
+        for r in picked:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 7:
+                continue
             try:
-                sm = float(r[1])
-                mx = float(r[2])
-                pw = float(r[3])
+                sms.append(float(f[0]))
+                mx = float(f[1])
             except ValueError:
                 continue
-            if pw > 200.0:       # under load
-                sms.append(sm)
-            for n, v in zip(names, r[5:9]):
-                if v.strip() == "Active":
+            for n, v in zip(self.NAMES, f[3:7]):
+                if v == "Active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sms) if sms else None, "sm_max_mhz": mx,
-                "samples_under_load": len(sms), "reasons": sorted(reasons)}
+                "samples": len(sms), "window": how, "reasons": sorted(reasons)}
 
 
 def file_sha(path):
@@ -225,18 +247,20 @@ def run_kvp(args):
 
     K = args.steps
     marks = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
-    with ClockSampler(local) as clk:
-        barrier()
-        torch.cuda.synchronize(dev)
-        launches0 = kvp.kvp_launch_count()
-        t_wall = time.perf_counter()
-        for s in range(K):
-            flush.zero_()                      # evict L2 (not timed: outside the marks)
-            step(marks[s])
-        torch.cuda.synchronize(dev)
-        t_wall = time.perf_counter() - t_wall
-        launches = kvp.kvp_launch_count() - launches0
-        barrier()
+    clk = ClockSampler(local).__enter__()
+    barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = kvp.kvp_launch_count()
+    t0 = time.time()
+    t_wall = time.perf_counter()
+    for s in range(K):
+        flush.zero_()                      # evict L2 (not timed: outside the marks)
+        step(marks[s])
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall
+    clk.mark(t0, time.time())
+    launches = kvp.kvp_launch_count() - launches0
+    barrier()
     kvp.kvp_check_device_status()
     stage_names = ["lse_pass", "future_attn_mass", "select_topk", "compact_kv", "decode_attn"]
     per_stage = {n: [] for n in stage_names}
@@ -284,6 +308,7 @@ def run_kvp(args):
         f_c, t_c, cores, desc = oracle_sample_time(w)
         cpu = {"value": f_c / t_c / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                "sample": desc, "seconds": t_c}
+    clk.__exit__(None, None, None)
     clocks = clk.summary()
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": K,
@@ -427,14 +452,72 @@ def e2e_measure(kvp, x, plan, budgets, w, K, W, stream, flops, ws, dev):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
+def run_ncu_case(args):
+    """A fixed case for profiler captures: `--steps` launches of one stage, no timing.
+    lse / fam: one Qwen3-4B-shaped layer at --seq-len (default 32768: Q = 256 MiB, larger than
+    L2); decode / select / compact: the Qwen2.5-1.5B decode-eviction shapes (T = 120000,
+    28 layers x 2 KV heads, budget 4096)."""
+    import learned_kv_cache_gb300 as kvp
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    kvp.load()
+    case = args.ncu_case
+    if case in ("lse", "fam"):
+        w = kvp_inputs.QWEN3_4B_LAYER.scaled(seq_len=args.seq_len)
+        x = kvp_inputs.make_prefill_layer(w, 0, device=dev)
+        q, k = x["q"][None].contiguous(), x["k"][None].contiguous()
+        lse = kvp.kvp_lse_pass(q, k)
+        F = kvp.kvp_future_attn_mass(q, k, lse, w.window)
+        for _ in range(args.steps):
+            if case == "lse":
+                kvp.kvp_lse_pass(q, k, lse=lse)
+            else:
+                kvp.kvp_future_attn_mass(q, k, lse, w.window, F=F)
+    else:
+        w = kvp_inputs.QWEN25_15B_DECODE
+        R, T, D, b = w.rows, w.seq_len, w.head_dim, max(w.decode_budgets)
+        gen = torch.Generator(device=dev).manual_seed(0)
+        if case == "decode":
+            q = torch.randn(w.n_layers, w.h_q, D, generator=gen, device=dev).half()
+            kc = torch.randn(R, b, D, generator=gen, device=dev).half()
+            vc = torch.randn(R, b, D, generator=gen, device=dev).half()
+            lens = torch.full((R,), b, dtype=torch.int32, device=dev)
+            for _ in range(args.steps):
+                kvp.kvp_decode_attn(q, kc, vc, lens)
+        elif case == "select":
+            scores = torch.rand(R, T, generator=gen, device=dev)
+            budgets = torch.full((R,), b, dtype=torch.int32, device=dev)
+            for _ in range(args.steps):
+                kvp.kvp_select_topk(scores, budgets, w.n_sink, w.n_recent, b)
+        elif case == "compact":
+            k = torch.randn(R, T, D, generator=gen, device=dev).half()
+            v = torch.randn(R, T, D, generator=gen, device=dev).half()
+            idx = torch.sort(torch.randperm(T, device=dev)[:b]).values.to(torch.int32)
+            idx = idx[None].repeat(R, 1).contiguous()
+            cnt = torch.full((R,), b, dtype=torch.int32, device=dev)
+            for _ in range(args.steps):
+                kvp.kvp_compact_kv(k, v, idx, cnt)
+        else:
+            raise SystemExit(f"unknown --ncu-case {case}")
+    torch.cuda.synchronize(dev)
+    kvp.kvp_check_device_status()
+    print(f"ncu case {case}: {args.steps} launches ok", flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kvp", choices=["kvp", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu-case", default=None,
+                    help="profiler case: lse | fam | decode | select | compact (no JSON line)")
+    ap.add_argument("--seq-len", type=int, default=32768)
     args = ap.parse_args()
+    if args.ncu_case:
+        return run_ncu_case(args)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
