@@ -128,6 +128,26 @@ __device__ __forceinline__ Item decode_item(int I, const TcParams& p) {
   return it;
 }
 
+// Packed fp32 pairs (sm_100 family): two lanes of arithmetic per instruction.
+__device__ __forceinline__ uint64_t pack2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -261,9 +281,20 @@ __global__ void __launch_bounds__(THREADS, 2)
     const int r = quad * 32 + lane;            // row of the A tile handled by this thread
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     float* nl2 = nl2_all + warp * 64;
-    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;   // mass pass partial sums
+    uint64_t acc01 = 0, acc23 = 0;                           // mass pass: packed fp32 pairs
     float m = -INFINITY, l = 0.f;                            // LSE pass running state
     bool ok = true;
+    const uint64_t c2x2 = pack2(p.c2, p.c2);
+    // Mass pass: the LSE of this lane's two columns, loaded one tile ahead.
+    float la = INFINITY, lb = INFINITY;
+    auto lse_load = [&](int t, float& x, float& y) {
+      const int gh = t / it.per_head, u = t % it.per_head;
+      const int ia = j0 + p.window + BN * (it.chunk * p.TPC + u) + half * 64 + 2 * lane;
+      const float* lrow = p.lse + (size_t)(b_of_group * p.Hq + hkv * p.G + gh) * p.S;
+      x = ia < p.S ? lrow[ia] : INFINITY;
+      y = ia + 1 < p.S ? lrow[ia + 1] : INFINITY;
+    };
+    if (MODE == 1 && it.n_tiles > 0) lse_load(0, la, lb);
     for (int t = 0; t < it.n_tiles; ++t) {
       const int a = t % NACC;
       if (!ptx::mbar_wait(bar_accf + 8 * a, (t / NACC) & 1, abort_flag, p.status)) { ok = false; break; }
@@ -297,26 +328,26 @@ __global__ void __launch_bounds__(THREADS, 2)
           l *= fast_exp2(m - mn);
           m = mn;
         }
-        const float nm = -m;
-        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+        const uint64_t nm2 = pack2(-m, -m);
+        uint64_t s01 = 0, s23 = 0;
 #pragma unroll
         for (int c = 0; c < 64; c += 4) {
-          s0 += fast_exp2(fmaf(__uint_as_float(v[c]), p.c2, nm));
-          s1 += fast_exp2(fmaf(__uint_as_float(v[c + 1]), p.c2, nm));
-          s2 += fast_exp2(fmaf(__uint_as_float(v[c + 2]), p.c2, nm));
-          s3 += fast_exp2(fmaf(__uint_as_float(v[c + 3]), p.c2, nm));
+          float x0, x1, x2, x3;
+          unpack2(ffma2(pack2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), c2x2, nm2), x0, x1);
+          unpack2(ffma2(pack2(__uint_as_float(v[c + 2]), __uint_as_float(v[c + 3])), c2x2, nm2), x2, x3);
+          s01 = fadd2(s01, pack2(fast_exp2(x0), fast_exp2(x1)));
+          s23 = fadd2(s23, pack2(fast_exp2(x2), fast_exp2(x3)));
         }
-        l += (s0 + s1) + (s2 + s3);
+        float q0, q1, q2, q3;
+        unpack2(s01, q0, q1);
+        unpack2(s23, q2, q3);
+        l += (q0 + q1) + (q2 + q3);
       } else {
-        const int gh = t / it.per_head, u = t % it.per_head;
-        const int i0 = j0 + p.window + BN * (it.chunk * p.TPC + u) + half * 64;
-        const float* lrow = p.lse + (size_t)(b_of_group * p.Hq + hkv * p.G + gh) * p.S;
-        {
-          const int ia = i0 + 2 * lane;
-          nl2[2 * lane] = ia < p.S ? -lrow[ia] * KVP_LOG2E : -INFINITY;
-          nl2[2 * lane + 1] = ia + 1 < p.S ? -lrow[ia + 1] * KVP_LOG2E : -INFINITY;
-        }
+        const int u = t % it.per_head;
+        nl2[2 * lane] = -la * KVP_LOG2E;          // lse = +inf past S -> weight 0
+        nl2[2 * lane + 1] = -lb * KVP_LOG2E;
         __syncwarp();
+        if (t + 1 < it.n_tiles) lse_load(t + 1, la, lb);
         const bool diag = (it.chunk == 0 && u == 0);
         if (diag) {
 #pragma unroll
@@ -327,10 +358,14 @@ __global__ void __launch_bounds__(THREADS, 2)
 #pragma unroll
         for (int c = 0; c < 64; c += 4) {
           const float4 n = n4[c >> 2];
-          acc0 += fast_exp2(fmaf(__uint_as_float(v[c]), p.c2, n.x));
-          acc1 += fast_exp2(fmaf(__uint_as_float(v[c + 1]), p.c2, n.y));
-          acc2 += fast_exp2(fmaf(__uint_as_float(v[c + 2]), p.c2, n.z));
-          acc3 += fast_exp2(fmaf(__uint_as_float(v[c + 3]), p.c2, n.w));
+          float x0, x1, x2, x3;
+          unpack2(ffma2(pack2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), c2x2, pack2(n.x, n.y)),
+                  x0, x1);
+          unpack2(ffma2(pack2(__uint_as_float(v[c + 2]), __uint_as_float(v[c + 3])), c2x2,
+                        pack2(n.z, n.w)),
+                  x2, x3);
+          acc01 = fadd2(acc01, pack2(fast_exp2(x0), fast_exp2(x1)));
+          acc23 = fadd2(acc23, pack2(fast_exp2(x2), fast_exp2(x3)));
         }
         __syncwarp();
       }
@@ -353,7 +388,10 @@ __global__ void __launch_bounds__(THREADS, 2)
         if (i < p.S) p.out[(size_t)it.group * p.S + i] = (M + __log2f(L)) * KVP_LN2;
       }
     } else {
-      const float f = (acc0 + acc1) + (acc2 + acc3);
+      float f0, f1, f2, f3;
+      unpack2(acc01, f0, f1);
+      unpack2(acc23, f2, f3);
+      const float f = (f0 + f1) + (f2 + f3);
       if (half == 1) red[r] = f;
       asm volatile("bar.sync 1, %0;" ::"r"(EPI_WARPS * 32));
       if (half == 0 && ok && !*abort_flag && it.n_tiles > 0) {

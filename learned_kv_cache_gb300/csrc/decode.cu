@@ -265,7 +265,9 @@ DecodePlan decode_plan(int n_layers, int h_q, int h_kv, int head_dim, int T_cap,
   p.partial_bytes = align256((size_t)p.R * p.n_chunks * p.G * (head_dim + 2) * sizeof(float));
   p.lse_bytes = align256((size_t)p.R * p.G * sizeof(float));
   p.logit_bytes = with_key_mass ? align256((size_t)p.R * p.G * T_cap * sizeof(float)) : 0;
-  p.total_bytes = p.partial_bytes + p.lse_bytes + p.logit_bytes;
+  p.simt_total_bytes = p.partial_bytes + p.lse_bytes + p.logit_bytes;
+  decode_mma_plan(p, head_dim, T_cap, with_key_mass);
+  p.total_bytes = p.simt_total_bytes > p.mma_total_bytes ? p.simt_total_bytes : p.mma_total_bytes;
   return p;
 }
 
@@ -298,12 +300,11 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, int dty
 #define KVP_DEC(TT, DD)                                                                            \
   return decode<TT, DD>(q, kc, vc, n_layers, h_q, h_kv, T_cap, len, scale, out, key_mass, key_pos, \
                         T_src, accumulate, plan, ws, status, st)
-  const bool d128 = head_dim == 128;
-  switch (dtype) {
-    case KVP_F32: if (d128) KVP_DEC(float, 128); else KVP_DEC(float, 64);
-    case KVP_BF16: if (d128) KVP_DEC(__nv_bfloat16, 128); else KVP_DEC(__nv_bfloat16, 64);
-    default: if (d128) KVP_DEC(__half, 128); else KVP_DEC(__half, 64);
-  }
+  if (dtype != KVP_F32)
+    return launch_decode_mma(q, kc, vc, dtype, n_layers, h_q, h_kv, head_dim, T_cap, len, scale, out,
+                             key_mass, key_pos, T_src, accumulate, plan, ws, status, st);
+  if (head_dim == 128) KVP_DEC(float, 128);
+  KVP_DEC(float, 64);
 #undef KVP_DEC
 }
 

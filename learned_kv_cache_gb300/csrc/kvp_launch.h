@@ -40,9 +40,21 @@ cudaError_t launch_compact(const void* k, const void* v, int row_bytes, int R, i
                            void* v_out, int* status, cudaStream_t st);
 
 struct DecodePlan {
-  int R, G, n_chunks, chunk;
-  size_t partial_bytes, lse_bytes, logit_bytes, total_bytes;
+  int R, G;
+  // fp32 cache path (grid of key chunks x rows)
+  int n_chunks, chunk;
+  size_t partial_bytes, lse_bytes, logit_bytes, simt_total_bytes;
+  // bf16/f16 cache path (persistent stream-K CTAs over 64-key tiles)
+  int nt, n_ctas, maxseg;
+  size_t mma_partial_bytes, counter_bytes, mma_lse_bytes, mma_logit_bytes, mma_total_bytes;
+  size_t total_bytes;   // workspace that covers either path
 };
+void decode_mma_plan(DecodePlan& p, int head_dim, int T_cap, int with_key_mass);
+cudaError_t launch_decode_mma(const void* q, const void* kc, const void* vc, int dtype, int n_layers,
+                              int h_q, int h_kv, int head_dim, int T_cap, const int32_t* len,
+                              float scale, float* out, float* key_mass, const int32_t* key_pos,
+                              int T_src, int accumulate, const DecodePlan& plan, void* ws,
+                              int* status, cudaStream_t st);
 DecodePlan decode_plan(int n_layers, int h_q, int h_kv, int head_dim, int T_cap, int with_key_mass);
 // Static scratch of kvp_decode_attn_noalloc on the current device (set up on first use).
 cudaError_t decode_noalloc_scratch(void** ptr, size_t* bytes);
