@@ -23,6 +23,8 @@
 // With the key mass requested, every logit is also stored ([R, T_cap, 8]) and a
 // second kernel adds the group-summed probability of each key at its source
 // position once the row's log-sum-exp is known.
+#include <cooperative_groups.h>
+
 #include "kvp_common.cuh"
 #include "kvp_launch.h"
 #include "tc_ptx.cuh"
@@ -47,7 +49,8 @@ struct Dm {
   static constexpr int OFF_BAR = STAGES * STAGE_BYTES;
   static constexpr int OFF_SM = OFF_BAR + 128;              // merge scratch
   static constexpr int SCRATCH = (2 * DM_CWARPS * DM_QPAD + DM_CWARPS * DM_QPAD * D) * 4;
-  static constexpr int OFF_FLAG = OFF_SM + SCRATCH;
+  static constexpr int OFF_CST = OFF_SM + SCRATCH;          // merged state of this CTA
+  static constexpr int OFF_FLAG = OFF_CST + PSTRIDE * 4;
   static constexpr int MAXC = (DM_CWARPS * DM_QPAD * D) / (2 + 2 * DM_QPAD);   // combine capacity
   static constexpr int SMEM = OFF_FLAG + 16 + 1024;         // + alignment slack
 };
@@ -64,6 +67,8 @@ struct DmParams {
   float* lse2;           // [R][8] (base-2 LSE per query head, for the key mass)
   float* logits;         // [R][T_cap][8] or null
   int* status;
+  int cluster;           // > 0: the `cluster` CTAs of a row form a thread-block cluster and
+                         // merge through distributed shared memory (no partials in HBM)
 };
 
 // First tile of CTA c, and the CTA that owns tile x (ranges are floor(c * total / P)).
@@ -157,6 +162,7 @@ __global__ void __launch_bounds__(DM_THREADS, 2)
   float* sm_l = sm_m + DM_CWARPS * DM_QPAD;                           // [4][8]
   float* sm_o = sm_l + DM_CWARPS * DM_QPAD;                           // [4][8][D]
   volatile int* flags = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);  // [0] abort, [1] last
+  float* cst = reinterpret_cast<float*>(smem + C::OFF_CST);          // m[8], l[8], o[8][D]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
@@ -170,6 +176,10 @@ __global__ void __launch_bounds__(DM_THREADS, 2)
     flags[0] = 0;
     flags[1] = 0;
     ptx::fence_mbar_init();
+  }
+  if (threadIdx.x < DM_QPAD) {
+    cst[threadIdx.x] = -INFINITY;
+    cst[DM_QPAD + threadIdx.x] = 0.f;
   }
   __syncthreads();
 
@@ -249,7 +259,7 @@ __global__ void __launch_bounds__(DM_THREADS, 2)
         ow[(2 * t + 1) * D + 16 * db + g + 8] = o[db][3];
       }
       asm volatile("bar.sync 1, %0;" ::"r"(DM_CWARPS * 32));
-      float* part = p.partial + ((size_t)c * p.maxseg + seg) * C::PSTRIDE;
+      float* part = p.cluster ? cst : p.partial + ((size_t)c * p.maxseg + seg) * C::PSTRIDE;
       for (int e = ctid; e < DM_QPAD * D; e += DM_CWARPS * 32) {
         const int qh = e / D, d = e % D;
         float M = -INFINITY;
@@ -270,6 +280,11 @@ __global__ void __launch_bounds__(DM_THREADS, 2)
           part[DM_QPAD + qh] = L;
         }
         part[2 * DM_QPAD + qh * D + d] = O;
+      }
+      if (p.cluster) {                       // merged at the end through distributed shared memory
+        asm volatile("bar.sync 1, %0;" ::"r"(DM_CWARPS * 32));
+        ++seg;
+        return;
       }
       __threadfence();
       asm volatile("bar.sync 1, %0;" ::"r"(DM_CWARPS * 32));
@@ -424,7 +439,42 @@ __global__ void __launch_bounds__(DM_THREADS, 2)
     }
     if (cur_row >= 0) finish_row(cur_row);
   }
-  __syncthreads();
+  if (p.cluster) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();                          // every CTA of the row has its state in shared memory
+    if (cluster.block_rank() == 0 && warp < DM_CWARPS) {
+      const int k = (int)cluster.num_blocks();
+      const int r = c / k, l = r / p.Hkv, hk = r % p.Hkv;
+      const float* rs[8];
+      for (int rr = 0; rr < k; ++rr) rs[rr] = cluster.map_shared_rank(cst, rr);
+      for (int e = threadIdx.x; e < p.G * D; e += DM_CWARPS * 32) {
+        const int qh = e / D, d = e % D;
+        float mr[8], M = -INFINITY;
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) {
+          mr[rr] = rr < k ? rs[rr][qh] : -INFINITY;
+          M = fmaxf(M, mr[rr]);
+        }
+        float L = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int rr = 0; rr < 8; ++rr) {
+            if (rr < k && mr[rr] != -INFINITY) {
+              const float wgt = fast_exp2(mr[rr] - M);
+              L = fmaf(rs[rr][DM_QPAD + qh], wgt, L);
+              O = fmaf(rs[rr][2 * DM_QPAD + qh * D + d], wgt, O);
+            }
+          }
+        }
+        p.out[((size_t)l * p.Hq + hk * p.G + qh) * D + d] = L > 0.f ? O / L : 0.f;
+        if (d == 0) p.lse2[r * DM_QPAD + qh] = L > 0.f ? M + __log2f(L) : -INFINITY;
+      }
+    }
+    cluster.sync();                          // remote reads are done before any CTA exits
+  } else {
+    __syncthreads();
+  }
 }
 
 // key_mass[r, pos(m)] (+)= sum_g exp2(logit[r, m, g] - lse2[r, g]) for m < len[r].
@@ -510,13 +560,31 @@ cudaError_t run(const void* q, const void* kc, const void* vc, int dtype, int n_
                       : nullptr;
   p.out = out;
   p.status = status;
-  cudaError_t e = cudaMemsetAsync(p.counters, 0, plan.counter_bytes, st);
-  if (e != cudaSuccess) return e;
+  const int k = plan.n_ctas / plan.R;
+  p.cluster = k <= 8 ? k : 0;
+  cudaError_t e = cudaSuccess;
+  if (!p.cluster) {
+    e = cudaMemsetAsync(p.counters, 0, plan.counter_bytes, st);
+    if (e != cudaSuccess) return e;
+  }
   auto kern = decode_mma_kernel<T, D>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Dm<D>::SMEM);
   if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)plan.n_ctas);
+  cfg.blockDim = dim3(DM_THREADS);
+  cfg.dynamicSmemBytes = Dm<D>::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.cluster ? p.cluster : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   count_launches(1);
-  kern<<<plan.n_ctas, DM_THREADS, Dm<D>::SMEM, st>>>(tk, tv, (const T*)q, p);
+  e = cudaLaunchKernelEx(&cfg, kern, tk, tv, (const T*)q, p);
+  if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess || !key_mass) return e;
   if (!accumulate) {
