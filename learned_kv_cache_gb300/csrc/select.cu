@@ -9,12 +9,14 @@
 // the sinks / recent window, and writes their indices in ascending order
 // through block-wide prefix scans.
 //
-// A row is handled by a thread-block cluster of up to 8 CTAs: each CTA keeps
-// the keys of its slice of the row in shared memory (one read of the scores
-// from HBM), the per-pass histograms are summed across the cluster through
-// distributed shared memory, and the tie ranks and output offsets come from
-// cluster-wide prefix counts.  Rows longer than 8 slices of shared memory use
-// the single-CTA kernel, which re-reads the row from L2 on every pass.
+// A row is handled by a thread-block cluster of up to 8 CTAs, each owning one
+// slice of the row: the radix passes start at the highest bit where the row's
+// keys differ (cluster-wide min / max), per-pass histograms (private to pairs
+// of warps) are summed across the
+// cluster through distributed shared memory, and the tie ranks and output
+// offsets come from cluster-wide prefix counts.  The order keys of a slice
+// (up to 16384) live in shared memory; longer slices recompute the rest from
+// the L2-resident scores on every pass.
 //
 // Soft-TopK (LKV "The Differentiable Soft-TopK Operator", "LKV-H"): one CTA
 // sorts the n <= 1024 head scores, forms the prefix sums S1 = sum exp(-x) and
@@ -37,14 +39,6 @@ __device__ __forceinline__ uint32_t order_key(float x) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-
-// Add 1 to hist[bin] for every active lane, one atomic per distinct bin per warp.
-__device__ __forceinline__ void hist_add(int* hist, uint32_t bin, bool active) {
-  const unsigned act = __ballot_sync(0xffffffffu, active);
-  if (!active) return;
-  const unsigned peers = __match_any_sync(act, bin);
-  if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
-}
 
 // Warp 0: the digit d whose bin holds the `remaining`-th largest key (bins scanned from 255
 // down), and how many keys of that bin are still needed.
@@ -75,113 +69,13 @@ __device__ __forceinline__ void pick_digit(const int* hist, int remaining, int* 
   }
 }
 
-constexpr int SEL_THREADS = 1024;
-constexpr int SEL_ITEMS = 4;              // consecutive tokens per thread in the output pass
-
-__global__ void __launch_bounds__(SEL_THREADS) select_kernel(
-    const float* __restrict__ scores, int T, long long row_stride, const int32_t* __restrict__ budgets,
-    int n_sink, int n_recent, int32_t* __restrict__ idx, int b_max, int32_t* __restrict__ count,
-    int* status) {
-  __shared__ int hist[256];
-  __shared__ int scan_sh[33];
-  __shared__ int sel_digit, sel_remaining;
-  const int r = blockIdx.x;
-  const float* s = scores + (size_t)r * row_stride;
-  int32_t* out = idx + (size_t)r * b_max;
-  const int b = budgets[r];
-  if (b < 0) {
-    if (threadIdx.x == 0) { count[r] = -1; raise_status(status, KVP_ERR_DEVICE_CHECK); }
-    return;
-  }
-  const int b_eff = (T <= b) ? T : min(T, max(b, n_sink + n_recent));
-  if (b_eff > b_max) {
-    if (threadIdx.x == 0) { count[r] = -1; raise_status(status, KVP_ERR_DEVICE_CHECK); }
-    return;
-  }
-  const bool keep_all = b_eff >= T;
-  const int mid_lo = n_sink, mid_hi = T - n_recent;
-  int k = keep_all ? 0 : b_eff - n_sink - n_recent;
-
-  uint32_t prefix = 0u, mask = 0u;
-  int remaining = k;
-  if (k > 0) {
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
-      __syncthreads();
-      for (int i0 = mid_lo; i0 < mid_hi; i0 += blockDim.x) {
-        const int i = i0 + threadIdx.x;
-        const uint32_t key = i < mid_hi ? order_key(s[i]) : 0u;
-        hist_add(hist, (key >> shift) & 255u, i < mid_hi && (key & mask) == prefix);
-      }
-      __syncthreads();
-      if (threadIdx.x < 32) pick_digit(hist, remaining, &sel_digit, &sel_remaining);
-      __syncthreads();
-      prefix |= (uint32_t)sel_digit << shift;
-      mask |= 255u << shift;
-      remaining = sel_remaining;
-      __syncthreads();
-    }
-  }
-  const uint32_t vstar = prefix;
-  // Output pass in token order.
-  int base = 0, eq_base = 0;
-  for (int c0 = 0; c0 < T; c0 += SEL_THREADS * SEL_ITEMS) {
-    const int i_first = c0 + threadIdx.x * SEL_ITEMS;
-    uint32_t keys[SEL_ITEMS];
-    int n_eq = 0;
-#pragma unroll
-    for (int t = 0; t < SEL_ITEMS; ++t) {
-      const int i = i_first + t;
-      keys[t] = 0u;
-      if (k > 0 && i < T && i >= mid_lo && i < mid_hi) {
-        keys[t] = order_key(s[i]);
-        n_eq += keys[t] == vstar;
-      }
-    }
-    int eq_tot;
-    int eq_rank = eq_base + block_exclusive_scan(n_eq, scan_sh, &eq_tot);
-    bool keep[SEL_ITEMS];
-    int n_keep = 0;
-#pragma unroll
-    for (int t = 0; t < SEL_ITEMS; ++t) {
-      const int i = i_first + t;
-      bool kp = false;
-      if (i < T) {
-        if (keep_all || i < mid_lo || i >= mid_hi) {
-          kp = true;
-        } else if (k > 0) {
-          if (keys[t] > vstar) kp = true;
-          else if (keys[t] == vstar) { kp = eq_rank < remaining; ++eq_rank; }
-        }
-      }
-      keep[t] = kp;
-      n_keep += kp;
-    }
-    int keep_tot;
-    int pos = base + block_exclusive_scan(n_keep, scan_sh, &keep_tot);
-#pragma unroll
-    for (int t = 0; t < SEL_ITEMS; ++t)
-      if (keep[t]) {
-        if (pos < b_max) out[pos] = i_first + t;
-        ++pos;
-      }
-    base += keep_tot;
-    eq_base += eq_tot;
-  }
-  for (int m = base + threadIdx.x; m < b_max; m += blockDim.x) out[m] = -1;
-  if (threadIdx.x == 0) {
-    count[r] = base;
-    if (base != b_eff) raise_status(status, KVP_ERR_DEVICE_CHECK);
-  }
-}
-
 // ---------------------------------------------------------------------------
 constexpr int SC_THREADS = 512;
-constexpr int SC_ITEMS = 4;
-constexpr int SC_MAX_SLICE = 16384;       // keys of one CTA's slice held in shared memory
 constexpr int SC_MAX_CLUSTER = 8;
+constexpr int SC_PRIV = 8;                // private histograms per CTA
+constexpr int SC_SMEM_KEYS = 16384;       // order keys of a slice held in shared memory (64 KB)
 
-__global__ void __launch_bounds__(SC_THREADS) select_cluster_kernel(
+__global__ void __launch_bounds__(SC_THREADS, 4) select_cluster_kernel(
     const float* __restrict__ scores, int T, long long row_stride, const int32_t* __restrict__ budgets,
     int n_sink, int n_recent, int32_t* __restrict__ idx, int b_max, int32_t* __restrict__ count,
     int* status) {
@@ -190,9 +84,12 @@ __global__ void __launch_bounds__(SC_THREADS) select_cluster_kernel(
   const int CL = (int)cluster.num_blocks();
   const int rank = (int)cluster.block_rank();
   const int r = blockIdx.x / CL;
-  extern __shared__ uint32_t keys[];
+  extern __shared__ uint32_t skeys[];    // [min(slice, SC_SMEM_KEYS)]
   __shared__ int hist[2][256];
   __shared__ int hsum[256];
+  __shared__ int priv[SC_PRIV][256];     // histograms private to pairs of warps
+  __shared__ uint32_t mm_sh[2][SC_THREADS / 32];
+  __shared__ uint32_t span[2];           // this CTA's smallest / largest middle key
   __shared__ int pub[2];                 // published counts: [0] ties, [1] kept
   __shared__ int scan_sh[33];
   __shared__ int sel_digit, sel_rem;
@@ -215,50 +112,129 @@ __global__ void __launch_bounds__(SC_THREADS) select_cluster_kernel(
   const int per = (T + CL - 1) / CL;
   const int lo = min(T, rank * per), hi = min(T, lo + per);
   const int nloc = hi - lo;
+  // The order keys of the slice are kept in shared memory (up to SC_SMEM_KEYS; keys past
+  // that are recomputed from the scores, which stay in L2 after the first pass).
+  const int nsm = min(nloc, SC_SMEM_KEYS);
   if (k > 0) {
-    // 8 independent loads in flight per thread before the keys are stored
     constexpr int U = 8;
-    for (int i0 = 0; i0 < nloc; i0 += U * SC_THREADS) {
+    for (int i0 = 0; i0 < nsm; i0 += U * SC_THREADS) {
       float v[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int i = i0 + u * SC_THREADS + tid;
-        v[u] = i < nloc ? __ldg(s + lo + i) : 0.f;
+        v[u] = i < nsm ? __ldg(s + lo + i) : 0.f;
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int i = i0 + u * SC_THREADS + tid;
-        if (i < nloc) keys[i] = order_key(v[u]);
+        if (i < nsm) skeys[i] = order_key(v[u]);
       }
     }
+    __syncthreads();
   }
-
+  auto key_at = [&](int i) { return i < SC_SMEM_KEYS ? skeys[i] : order_key(__ldg(s + lo + i)); };
   uint32_t prefix = 0u, mask = 0u;
   int remaining = k;
   if (k > 0) {
-    for (int pass = 0; pass < 4; ++pass) {
-      const int shift = 24 - 8 * pass;
-      int* h = hist[pass & 1];
-      for (int i = tid; i < 256; i += blockDim.x) h[i] = 0;
-      __syncthreads();
-      for (int i0 = 0; i0 < nloc; i0 += blockDim.x) {
-        const int i = i0 + tid, gi = lo + i;
-        const bool in = i < nloc && gi >= mid_lo && gi < mid_hi;
-        const uint32_t key = in ? keys[i] : 0u;
-        hist_add(h, (key >> shift) & 255u, in && (key & mask) == prefix);
+    // The bits above the highest bit where the row's smallest and largest middle keys differ
+    // are common to every key: the radix passes start below them.
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    for (int i = tid; i < nloc; i += blockDim.x) {
+      const int gi = lo + i;
+      if (gi >= mid_lo && gi < mid_hi) {
+        const uint32_t key = key_at(i);
+        kmin = min(kmin, key);
+        kmax = max(kmax, key);
       }
-      cluster.sync();
-      for (int i = tid; i < 256; i += blockDim.x) {
-        int tot = 0;
-        for (int qr = 0; qr < CL; ++qr) tot += cluster.map_shared_rank(h, qr)[i];
-        hsum[i] = tot;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, off));
+      kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, off));
+    }
+    if ((tid & 31) == 0) {
+      mm_sh[0][tid >> 5] = kmin;
+      mm_sh[1][tid >> 5] = kmax;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      for (int w = 1; w < (int)(blockDim.x >> 5); ++w) {
+        kmin = min(kmin, mm_sh[0][w]);
+        kmax = max(kmax, mm_sh[1][w]);
       }
-      __syncthreads();
-      if (tid < 32) pick_digit(hsum, remaining, &sel_digit, &sel_rem);
-      __syncthreads();
-      prefix |= (uint32_t)sel_digit << shift;
-      mask |= 255u << shift;
-      remaining = sel_rem;
+      span[0] = kmin;
+      span[1] = kmax;
+    }
+    cluster.sync();
+    uint32_t gmin = 0xffffffffu, gmax = 0u;
+    {
+      uint32_t lo_v[SC_MAX_CLUSTER], hi_v[SC_MAX_CLUSTER];
+#pragma unroll
+      for (int qr = 0; qr < SC_MAX_CLUSTER; ++qr) {
+        const uint32_t* rs = cluster.map_shared_rank(&span[0], qr < CL ? qr : 0);
+        lo_v[qr] = rs[0];
+        hi_v[qr] = rs[1];
+      }
+#pragma unroll
+      for (int qr = 0; qr < SC_MAX_CLUSTER; ++qr) {
+        gmin = min(gmin, lo_v[qr]);
+        gmax = max(gmax, hi_v[qr]);
+      }
+    }
+    const uint32_t diff = gmin ^ gmax;
+    if (diff == 0u) {
+      prefix = gmin;                       // every middle key is equal
+      mask = 0xffffffffu;
+    } else {
+      int hi = 31 - __clz(diff);
+      mask = hi == 31 ? 0u : ~((2u << hi) - 1u);
+      prefix = gmin & mask;
+      for (int pass = 0; hi >= 0; ++pass) {
+        const int lo_bit = hi >= 7 ? hi - 7 : 0;
+        const uint32_t dmask = (1u << (hi - lo_bit + 1)) - 1u;
+        int* h = hist[pass & 1];
+        for (int i = tid; i < SC_PRIV * 256; i += blockDim.x) (&priv[0][0])[i] = 0;
+        __syncthreads();
+        int* mine = priv[(tid >> 5) % SC_PRIV];
+        constexpr int U = 4;                 // independent loads in flight per thread
+        for (int i0 = 0; i0 < nloc; i0 += U * SC_THREADS) {
+          uint32_t kk[U];
+          bool in[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int i = i0 + u * SC_THREADS + tid, gi = lo + i;
+            in[u] = i < nloc && gi >= mid_lo && gi < mid_hi;
+            kk[u] = in[u] ? key_at(i) : 0u;
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+            if (in[u] && (kk[u] & mask) == prefix) atomicAdd(&mine[(kk[u] >> lo_bit) & dmask], 1);
+        }
+        __syncthreads();
+        for (int i = tid; i < 256; i += blockDim.x) {
+          int tot = 0;
+#pragma unroll
+          for (int j = 0; j < SC_PRIV; ++j) tot += priv[j][i];
+          h[i] = tot;
+        }
+        cluster.sync();
+        if (tid < 256) {                   // all remote loads in flight at once
+          int v[SC_MAX_CLUSTER];
+#pragma unroll
+          for (int qr = 0; qr < SC_MAX_CLUSTER; ++qr) v[qr] = qr < CL ? cluster.map_shared_rank(h, qr)[tid] : 0;
+          int tot = 0;
+#pragma unroll
+          for (int qr = 0; qr < SC_MAX_CLUSTER; ++qr) tot += v[qr];
+          hsum[tid] = tot;
+        }
+        __syncthreads();
+        if (tid < 32) pick_digit(hsum, remaining, &sel_digit, &sel_rem);
+        __syncthreads();
+        prefix |= (uint32_t)sel_digit << lo_bit;
+        mask |= dmask << lo_bit;
+        remaining = sel_rem;
+        hi = lo_bit - 1;
+      }
     }
   }
   const uint32_t vstar = prefix;
@@ -270,8 +246,9 @@ __global__ void __launch_bounds__(SC_THREADS) select_cluster_kernel(
     if (keep_all || gi < mid_lo || gi >= mid_hi) {
       ++n_fixed;
     } else if (k > 0) {
-      n_eq += keys[i] == vstar;
-      n_gt += keys[i] > vstar;
+      const uint32_t key = key_at(i);
+      n_eq += key == vstar;
+      n_gt += key > vstar;
     }
   }
   int tot;
@@ -284,55 +261,66 @@ __global__ void __launch_bounds__(SC_THREADS) select_cluster_kernel(
   if (tid == 0) pub[0] = n_eq;
   cluster.sync();
   int eq_before = 0;
-  for (int qr = 0; qr < rank; ++qr) eq_before += *cluster.map_shared_rank(&pub[0], qr);
+#pragma unroll
+  for (int qr = 0; qr < SC_MAX_CLUSTER; ++qr) {
+    const int v = *cluster.map_shared_rank(&pub[0], qr < CL ? qr : 0);
+    eq_before += qr < rank ? v : 0;
+  }
   const int eq_keep = k > 0 ? max(0, min(n_eq, remaining - eq_before)) : 0;
   if (tid == 0) pub[1] = n_fixed + n_gt + eq_keep;
   cluster.sync();
-  int base = 0;
-  for (int qr = 0; qr < rank; ++qr) base += *cluster.map_shared_rank(&pub[1], qr);
-  int total_kept = 0;
-  for (int qr = 0; qr < CL; ++qr) total_kept += *cluster.map_shared_rank(&pub[1], qr);
+  int base = 0, total_kept = 0;
+#pragma unroll
+  for (int qr = 0; qr < SC_MAX_CLUSTER; ++qr) {
+    const int v = *cluster.map_shared_rank(&pub[1], qr < CL ? qr : 0);
+    base += qr < rank ? v : 0;
+    total_kept += qr < CL ? v : 0;
+  }
   cluster.sync();                        // no CTA leaves while others read its counts
 
-  // Write the kept indices of this slice in token order.
-  int eq_base = eq_before;
-  for (int c0 = 0; c0 < nloc; c0 += SC_THREADS * SC_ITEMS) {
-    const int i_first = c0 + tid * SC_ITEMS;
+  // Write the kept indices of this slice in token order: thread t owns one contiguous run,
+  // so two block scans give every thread its tie rank and its output position.
+  {
+    const int run = (nloc + (int)blockDim.x - 1) / (int)blockDim.x;
+    const int a = min(nloc, tid * run), z = min(nloc, a + run);
     int ne = 0;
-#pragma unroll
-    for (int t = 0; t < SC_ITEMS; ++t) {
-      const int i = i_first + t, gi = lo + i;
-      if (k > 0 && i < nloc && gi >= mid_lo && gi < mid_hi) ne += keys[i] == vstar;
-    }
-    int etot;
-    int eq_rank = eq_base + block_exclusive_scan(ne, scan_sh, &etot);
-    bool kp[SC_ITEMS];
-    int nk = 0;
-#pragma unroll
-    for (int t = 0; t < SC_ITEMS; ++t) {
-      const int i = i_first + t, gi = lo + i;
-      bool v = false;
-      if (i < nloc) {
-        if (keep_all || gi < mid_lo || gi >= mid_hi) {
-          v = true;
-        } else if (k > 0) {
-          if (keys[i] > vstar) v = true;
-          else if (keys[i] == vstar) { v = eq_rank < remaining; ++eq_rank; }
-        }
+    if (k > 0)
+      for (int i = a; i < z; ++i) {
+        const int gi = lo + i;
+        if (gi >= mid_lo && gi < mid_hi) ne += key_at(i) == vstar;
       }
-      kp[t] = v;
-      nk += v;
+    int etot;
+    int eq_rank = eq_before + block_exclusive_scan(ne, scan_sh, &etot);
+    const int eq_first = eq_rank;
+    int nk = 0;
+    for (int i = a; i < z; ++i) {
+      const int gi = lo + i;
+      if (keep_all || gi < mid_lo || gi >= mid_hi) {
+        ++nk;
+      } else if (k > 0) {
+        const uint32_t key = key_at(i);
+        if (key > vstar) ++nk;
+        else if (key == vstar) { nk += eq_rank < remaining; ++eq_rank; }
+      }
     }
     int ktot;
     int pos = base + block_exclusive_scan(nk, scan_sh, &ktot);
-#pragma unroll
-    for (int t = 0; t < SC_ITEMS; ++t)
-      if (kp[t]) {
-        if (pos < b_max) out[pos] = lo + i_first + t;
+    eq_rank = eq_first;
+    for (int i = a; i < z; ++i) {
+      const int gi = lo + i;
+      bool v = false;
+      if (keep_all || gi < mid_lo || gi >= mid_hi) {
+        v = true;
+      } else if (k > 0) {
+        const uint32_t key = key_at(i);
+        if (key > vstar) v = true;
+        else if (key == vstar) { v = eq_rank < remaining; ++eq_rank; }
+      }
+      if (v) {
+        if (pos < b_max) out[pos] = gi;
         ++pos;
       }
-    base += ktot;
-    eq_base += etot;
+    }
   }
   for (int m = total_kept + rank * blockDim.x + tid; m < b_max; m += CL * blockDim.x) out[m] = -1;
   if (rank == 0 && tid == 0) {
@@ -424,16 +412,10 @@ cudaError_t launch_select(const float* scores, int R, int T, int64_t row_stride,
   int cl = 1;
   while (cl < SC_MAX_CLUSTER && T / (2 * cl) >= 1024) cl *= 2;
   const int per = (T + cl - 1) / cl;
-  if (per > SC_MAX_SLICE) {
-    count_launches(1);
-    select_kernel<<<R, SEL_THREADS, 0, st>>>(scores, T, (long long)row_stride, budgets, n_sink,
-                                             n_recent, idx, b_max, count, status);
-    return cudaGetLastError();
-  }
-  const size_t smem = (size_t)per * sizeof(uint32_t);
-  cudaError_t e = cudaFuncSetAttribute(select_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e != cudaSuccess) return e;
+  const size_t smem = (size_t)(per < SC_SMEM_KEYS ? per : SC_SMEM_KEYS) * sizeof(uint32_t);
+  cudaError_t e0 = cudaFuncSetAttribute(select_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)smem);
+  if (e0 != cudaSuccess) return e0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(R * cl));
   cfg.blockDim = dim3(SC_THREADS);
@@ -446,6 +428,7 @@ cudaError_t launch_select(const float* scores, int R, int T, int64_t row_stride,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  cudaError_t e;
   count_launches(1);
   e = cudaLaunchKernelEx(&cfg, select_cluster_kernel, scores, T, (long long)row_stride, budgets, n_sink,
                          n_recent, idx, b_max, count, status);
