@@ -53,6 +53,26 @@ def dist_env():
     return ws, rank, local
 
 
+def rank_workload(w, rank):
+    """The independent layer a rank processes under weak scaling (its own seed)."""
+    return w.scaled(seed=w.seed + 100 * rank)
+
+
+def reduce_max(value, world_size, device=None):
+    """Max over ranks of a per-rank time (the slowest rank sets the step time)."""
+    if world_size <= 1:
+        return float(value)
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank, world_size, ms_per_step):
+    """Whole-job throughput: the work of all ranks over the (max-reduced) step time."""
+    return flops_per_rank * world_size / (ms_per_step / 1e3) / 1e12
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -220,7 +240,7 @@ def run_kvp(args):
     peaks, peak_src = load_peaks()
     w = kvp_inputs.QWEN3_4B_LAYER
     R, S, D = w.rows, w.seq_len, w.head_dim
-    x = kvp_inputs.make_prefill_layer(w.scaled(seed=w.seed + 100 * rank), 0, device=dev)
+    x = kvp_inputs.make_prefill_layer(rank_workload(w, rank), 0, device=dev)
     x = {k: v.unsqueeze(0).contiguous() for k, v in x.items()}
     plan = PrefillPrunePlan(1, w.h_q, w.h_kv, S, D, x["q"].dtype, w.window, w.n_sink, w.n_recent,
                             w.budget, device=dev)
@@ -283,17 +303,12 @@ def run_kvp(args):
         for i, n in enumerate(stage_names):
             per_stage[n].append(m[i].elapsed_time(m[i + 1]))
         step_ms.append(m[0].elapsed_time(m[5]))
-    ms = sum(step_ms) / K
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(sum(step_ms) / K, ws, dev)
     lse_flops = 2.0 * D * w.h_q * (S * (S + 1) // 2)
     ww = S - w.window
     fam_flops = 2.0 * D * w.h_q * (ww * (ww + 1) // 2)
     flops = lse_flops + fam_flops
-    value = flops * ws / (ms / 1e3) / 1e12
+    value = whole_job_tflops(flops, ws, ms)
     stage_mean = {n: sum(v) / K for n, v in per_stage.items()}
 
     # dominant kernel roofline
