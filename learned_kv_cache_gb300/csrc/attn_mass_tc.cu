@@ -54,17 +54,40 @@ constexpr int TILE_BYTES = 128 * HD * 2;         // 32 KB: two 128-row x 128-byt
 constexpr int HALF_BYTES = TILE_BYTES / 2;
 constexpr int TMEM_COLS = NACC * BN;             // 256
 
+constexpr int EXT_K = 16;                        // extra MMA K-step of the mass pass
+constexpr int EXT_BYTES = 128 * EXT_K * 2;       // one [128 x 16] 16-bit operand (4 KB)
+
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + TILE_BYTES;
 constexpr int OFF_BAR = OFF_B + NSTAGE * TILE_BYTES;
 constexpr int OFF_MISC = OFF_BAR + 256;
-constexpr int OFF_NL2 = OFF_MISC + 64;
-constexpr int OFF_RED = OFF_NL2 + EPI_WARPS * 64 * 4;
-constexpr int SMEM_BYTES = OFF_RED + 2 * BM * 4 * 2 + 1024;   // + alignment slack
+constexpr int OFF_AEXT = OFF_MISC + 256;         // key-side extension: [1, 1, 1, 0, ...] per row
+constexpr int OFF_BEXT = OFF_AEXT + EXT_BYTES;   // query-side extension per stage: -lse/scale split
+constexpr int OFF_RED = OFF_BEXT + NSTAGE * EXT_BYTES;
+constexpr int SMEM_BYTES = OFF_RED + 2 * BM * 4 + 1024;   // + alignment slack
+
+// Byte offset of element (r, k) of a [128 x 16] K-major operand in 8 x 16-byte core matrices
+// (core (r/8, k/8) at (r/8)*256 + (k/8)*128): the layout desc_noswz(addr, 128, 256) reads.
+__device__ __forceinline__ int ext_off(int r, int k) {
+  return (r >> 3) * 256 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
+}
+
+// Round to bf16 / f16 (bits) and return the value kept.
+__device__ __forceinline__ uint16_t round16(float x, bool bf16, float& kept) {
+  if (bf16) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    kept = __bfloat162float(h);
+    return *reinterpret_cast<const uint16_t*>(&h);
+  }
+  const __half h = __float2half_rn(x);
+  kept = __half2float(h);
+  return *reinterpret_cast<const uint16_t*>(&h);
+}
 
 struct TcParams {
   int S, Hq, Hkv, G;
   float c2;              // sm_scale * log2(e)
+  float inv_scale;       // 1 / sm_scale
   int window;
   const float* lse;      // mass pass: natural-log row LSE [B*Hq*S]
   float* out;            // LSE pass: lse [B*Hq*S]; mass pass: partial sums (workspace)
@@ -170,8 +193,9 @@ __global__ void __launch_bounds__(THREADS, 2)
   const uint32_t bar_a = bar_acce + 8 * NACC;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
-  float* nl2_all = reinterpret_cast<float*>(smem + OFF_NL2);
   float* red = reinterpret_cast<float*>(smem + OFF_RED);
+  const uint32_t sAext = s_base + OFF_AEXT;
+  const uint32_t sBext = s_base + OFF_BEXT;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Item it = decode_item<MODE>(blockIdx.x, p);
@@ -196,6 +220,20 @@ __global__ void __launch_bounds__(THREADS, 2)
   if (warp == PRODUCER_WARP && lane == 0) {
     ptx::prefetch_tmap(&tmQ);
     ptx::prefetch_tmap(&tmK);
+  }
+  if (MODE == 1 && threadIdx.x < EPI_WARPS * 32) {
+    // The extra K-step adds -lse_i/scale (B side, three 16-bit parts) times 1 (A side) to every
+    // logit, so the accumulator already holds the LSE-offset logit.
+    const uint16_t one = bf16 ? 0x3F80u : 0x3C00u;
+    for (int e = threadIdx.x; e < 128 * EXT_K; e += EPI_WARPS * 32) {
+      const int r = e / EXT_K, k = e % EXT_K;
+      *reinterpret_cast<uint16_t*>(smem + OFF_AEXT + ext_off(r, k)) = k < 3 ? one : 0u;
+    }
+    for (int e = threadIdx.x; e < NSTAGE * 128 * EXT_K; e += EPI_WARPS * 32) {
+      const int st = e / (128 * EXT_K), rem = e % (128 * EXT_K);
+      *reinterpret_cast<uint16_t*>(smem + OFF_BEXT + st * EXT_BYTES + ext_off(rem / EXT_K, rem % EXT_K)) = 0u;
+    }
+    ptx::fence_proxy_async_smem();
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -228,16 +266,50 @@ __global__ void __launch_bounds__(THREADS, 2)
   };
 
   if (warp == PRODUCER_WARP) {
+    const CUtensorMap* tmA = MODE == 0 ? &tmQ : &tmK;
+    const CUtensorMap* tmB = MODE == 0 ? &tmK : &tmQ;
     if (lane == 0) {
-      const CUtensorMap* tmA = MODE == 0 ? &tmQ : &tmK;
-      const CUtensorMap* tmB = MODE == 0 ? &tmK : &tmQ;
       ptx::mbar_arrive_expect_tx(bar_a, TILE_BYTES);
       ptx::tma_load_3d(sA, tmA, bar_a, 0, a_row, a_z);
       ptx::tma_load_3d(sA + HALF_BYTES, tmA, bar_a, 64, a_row, a_z);
-      int t = 0;
-      for (; t < it.n_tiles; ++t) {
-        const int s = t % NSTAGE, use = t / NSTAGE;
-        if (use > 0 && !ptx::mbar_wait(bar_empty + 8 * s, (use - 1) & 1, abort_flag, p.status)) break;
+    }
+    int t = 0;
+    for (; t < it.n_tiles; ++t) {
+      const int s = t % NSTAGE, use = t / NSTAGE;
+      float lv[4];
+      if (MODE == 1) {   // LSE of this tile's 128 queries, 4 per lane, loaded before the wait
+        const int gh = t / it.per_head, u = t % it.per_head;
+        const int i0 = j0 + p.window + BN * (it.chunk * p.TPC + u) + 4 * lane;
+        const float* lrow = p.lse + (size_t)(b_of_group * p.Hq + hkv * p.G + gh) * p.S;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) lv[j] = i0 + j < p.S ? __ldg(lrow + i0 + j) : INFINITY;
+      }
+      bool ok = true;
+      if (use > 0) ok = ptx::mbar_wait(bar_empty + 8 * s, (use - 1) & 1, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      if (MODE == 1) {
+        uint8_t* ext = smem + OFF_BEXT + s * EXT_BYTES;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = 4 * lane + j;
+          uint16_t h1, h2 = 0, h3 = 0;
+          if (lv[j] == INFINITY) {                 // query past S: weight exactly 0
+            h1 = bf16 ? 0xFF80u : 0xFC00u;         // -inf
+          } else {
+            const float h = -lv[j] * p.inv_scale;
+            float k1, k2, k3;
+            h1 = round16(h, bf16, k1);
+            h2 = round16(h - k1, bf16, k2);
+            h3 = round16((h - k1) - k2, bf16, k3);
+          }
+          *reinterpret_cast<uint16_t*>(ext + ext_off(r, 0)) = h1;
+          *reinterpret_cast<uint16_t*>(ext + ext_off(r, 1)) = h2;
+          *reinterpret_cast<uint16_t*>(ext + ext_off(r, 2)) = h3;
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+      }
+      if (lane == 0) {
         int row, z;
         b_coords(t, row, z);
         const uint32_t dst = sB + s * TILE_BYTES;
@@ -245,7 +317,9 @@ __global__ void __launch_bounds__(THREADS, 2)
         ptx::tma_load_3d(dst, tmB, bar_full + 8 * s, 0, row, z);
         ptx::tma_load_3d(dst + HALF_BYTES, tmB, bar_full + 8 * s, 64, row, z);
       }
-      // Let every copy this thread started land before the CTA can exit.
+    }
+    if (lane == 0) {
+      // Let every copy this warp started land before the CTA can exit.
       ptx::mbar_wait(bar_a, 0, abort_flag, p.status);
       for (int q = max(0, t - NSTAGE); q < t; ++q)
         ptx::mbar_wait(bar_full + 8 * (q % NSTAGE), (q / NSTAGE) & 1, abort_flag, p.status);
@@ -268,6 +342,9 @@ __global__ void __launch_bounds__(THREADS, 2)
             const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
             ptx::mma_f16_ss(d, ptx::desc_sw128(sA + off), ptx::desc_sw128(bs + off), idesc, kk > 0);
           }
+          if (MODE == 1)
+            ptx::mma_f16_ss(d, ptx::desc_noswz(sAext, 128, 256), ptx::desc_noswz(sBext + s * EXT_BYTES, 128, 256),
+                            idesc, 1);
           ptx::mma_commit(bar_empty + 8 * s);
           ptx::mma_commit(bar_accf + 8 * a);
         }
@@ -280,21 +357,10 @@ __global__ void __launch_bounds__(THREADS, 2)
     const int half = warp >> 2, quad = warp & 3;
     const int r = quad * 32 + lane;            // row of the A tile handled by this thread
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    float* nl2 = nl2_all + warp * 64;
     uint64_t acc01 = 0, acc23 = 0;                           // mass pass: packed fp32 pairs
     float m = -INFINITY, l = 0.f;                            // LSE pass running state
     bool ok = true;
     const uint64_t c2x2 = pack2(p.c2, p.c2);
-    // Mass pass: the LSE of this lane's two columns, loaded one tile ahead.
-    float la = INFINITY, lb = INFINITY;
-    auto lse_load = [&](int t, float& x, float& y) {
-      const int gh = t / it.per_head, u = t % it.per_head;
-      const int ia = j0 + p.window + BN * (it.chunk * p.TPC + u) + half * 64 + 2 * lane;
-      const float* lrow = p.lse + (size_t)(b_of_group * p.Hq + hkv * p.G + gh) * p.S;
-      x = ia < p.S ? lrow[ia] : INFINITY;
-      y = ia + 1 < p.S ? lrow[ia + 1] : INFINITY;
-    };
-    if (MODE == 1 && it.n_tiles > 0) lse_load(0, la, lb);
     for (int t = 0; t < it.n_tiles; ++t) {
       const int a = t % NACC;
       if (!ptx::mbar_wait(bar_accf + 8 * a, (t / NACC) & 1, abort_flag, p.status)) { ok = false; break; }
@@ -343,27 +409,20 @@ __global__ void __launch_bounds__(THREADS, 2)
         unpack2(s23, q2, q3);
         l += (q0 + q1) + (q2 + q3);
       } else {
+        // the accumulator holds (q.k - lse_i/scale); past S it is -inf
         const int u = t % it.per_head;
-        nl2[2 * lane] = -la * KVP_LOG2E;          // lse = +inf past S -> weight 0
-        nl2[2 * lane + 1] = -lb * KVP_LOG2E;
-        __syncwarp();
-        if (t + 1 < it.n_tiles) lse_load(t + 1, la, lb);
         const bool diag = (it.chunk == 0 && u == 0);
         if (diag) {
 #pragma unroll
           for (int c = 0; c < 64; ++c)
             if (half * 64 + c < r) v[c] = __float_as_uint(-INFINITY);
         }
-        const float4* n4 = reinterpret_cast<const float4*>(nl2);
+        const uint64_t zero2 = 0;
 #pragma unroll
         for (int c = 0; c < 64; c += 4) {
-          const float4 n = n4[c >> 2];
           float x0, x1, x2, x3;
-          unpack2(ffma2(pack2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), c2x2, pack2(n.x, n.y)),
-                  x0, x1);
-          unpack2(ffma2(pack2(__uint_as_float(v[c + 2]), __uint_as_float(v[c + 3])), c2x2,
-                        pack2(n.z, n.w)),
-                  x2, x3);
+          unpack2(ffma2(pack2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), c2x2, zero2), x0, x1);
+          unpack2(ffma2(pack2(__uint_as_float(v[c + 2]), __uint_as_float(v[c + 3])), c2x2, zero2), x2, x3);
           acc01 = fadd2(acc01, pack2(fast_exp2(x0), fast_exp2(x1)));
           acc23 = fadd2(acc23, pack2(fast_exp2(x2), fast_exp2(x3)));
         }
@@ -537,6 +596,7 @@ cudaError_t launch_fam_tc(const void* q, const void* k, const float* lse, int dt
   p.Hkv = s.h_kv;
   p.G = s.h_q / s.h_kv;
   p.c2 = scale * KVP_LOG2E;
+  p.inv_scale = 1.0f / scale;
   p.window = window;
   p.lse = lse;
   p.out = (float*)ws;

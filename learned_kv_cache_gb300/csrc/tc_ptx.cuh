@@ -146,6 +146,22 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t smem_addr) {
   return d;
 }
 
+// Shared-memory matrix descriptor of a K-major operand without swizzle, stored as 8-row x
+// 16-byte core matrices: `lbo` bytes between core matrices along K, `sbo` bytes between core
+// matrices along M (or N).
+__device__ __forceinline__ uint64_t desc_noswz(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;                              // descriptor version; swizzle bits 0 = none
+  return d;
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Instruction descriptor of kind::f16 with fp32 accumulation, both operands K-major.
 __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N) {
   return (1u << 4)                              // D format: f32
