@@ -43,7 +43,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM traffic of one launch of the dominant kernel from an ncu capture, valid only while the
 # kernel source is unchanged (sha256 of the .cu file at capture time).
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on this bench command, launches 7-10
+    # (profiles/traffic_bench_step.md): 117.24 / 116.44 MB read + 0.32 / 0.23 MB written
+    "future_attn_mass": {"sha": "901c9dcf0bcea0f1", "bytes": int((117244160 + 116442368 + 318208 + 226560) / 2)},
+}
 
 
 def dist_env():
