@@ -7,8 +7,9 @@ seeded inputs come from ``kvp_inputs``.
 
 Functions and the passages they follow:
 
-* :func:`row_lse`, :func:`future_attn_mass` -- KVpop, "Defining Future
-  Attention Utility", "Delayed Memory Scoring" and Figure 2.
+* :func:`row_lse`, :func:`future_attn_mass`, :func:`future_attn_mass_per_head`,
+  :func:`kvpop_target` -- KVpop, "Defining Future Attention Utility", "Delayed
+  Memory Scoring", "Alternative Aggregation Methods" and Figure 2.
 * :func:`select_topk`, :func:`compact_kv` -- KVpop "The KVpop Scoring Module";
   Learning to Evict from Key-Value Cache §1, §4.1, §A.2; How much KV cache can
   you prune, "What we did" and "Conclusion".
@@ -20,12 +21,12 @@ Every function is pinned by the ``-m "not gpu"`` tests (brute force through
 library softmax/logsumexp on tiny inputs, closed forms, invariants and the
 pages' worked examples).
 """
-from .attention_mass import future_attn_mass, row_lse
+from .attention_mass import future_attn_mass, future_attn_mass_per_head, kvpop_target, row_lse
 from .budgets import head_budgets, soft_topk
 from .decode import decode_attn
 from .selection import compact_kv, effective_budget, select_row, select_topk
 
 __all__ = [
-    "row_lse", "future_attn_mass", "select_topk", "select_row", "effective_budget",
+    "row_lse", "future_attn_mass", "future_attn_mass_per_head", "kvpop_target", "select_topk", "select_row", "effective_budget",
     "compact_kv", "decode_attn", "soft_topk", "head_budgets",
 ]

@@ -102,3 +102,43 @@ def future_attn_mass(q, k, lse, scale: float, window: int, keys=None) -> np.ndar
                     acc += np.where(after_window, p, 0.0).sum(axis=0)
             F[h, a:a + jj.size] = acc
     return F
+
+
+def future_attn_mass_per_head(q, k, lse, scale: float, window: int) -> np.ndarray:
+    """F_g[h_q, j] = sum_{i = j + w}^{S-1} exp(scale * q[h_q, i] . k[h_q // G, j] - lse[h_q, i]):
+    the future-attention mass of every key from each query head separately (KVpop, "Defining
+    Future Attention Utility": the mass is formed per query head g before the group
+    aggregation)."""
+    q = _as_f64(q)
+    k = _as_f64(k)
+    lse = _as_f64(lse)
+    Hq, S, _ = q.shape
+    G = Hq // k.shape[0]
+    out = np.zeros((Hq, S))
+    for hq in range(Hq):
+        out[hq] = future_attn_mass(q[hq:hq + 1], k[hq // G:hq // G + 1], lse[hq:hq + 1], scale, window)[0]
+    return out
+
+
+def kvpop_target(F_heads, window: int, group: int, eps: float = 0.0, aggregate: str = "max_log"):
+    """KVpop's supervision target from per-query-head future mass (KVpop, "Defining Future
+    Attention Utility", worked example, and "Alternative Aggregation Methods"):
+
+        N_t = max(1, S - (t + w))                 count normalisation
+        m_g(t) = F_g(t) / N_t                      mean future attention of query head g
+        max_log:   r(h, t) = max_g log(eps + m_g(t))
+        mean_prob: r(h, t) = log(eps + (1/G) sum_g m_g(t))   (the probability-space mean)
+
+    F_heads: [H_q, S] -> r: [H_q // G, S]."""
+    F = np.asarray(F_heads, dtype=np.float64)
+    Hq, S = F.shape
+    t = np.arange(S)
+    N = np.maximum(1, S - (t + window)).astype(np.float64)
+    m = F / N[None, :]
+    m = m.reshape(Hq // group, group, S)
+    with np.errstate(divide="ignore"):
+        if aggregate == "max_log":
+            return np.log(eps + m).max(axis=1)
+        if aggregate == "mean_prob":
+            return np.log(eps + m.mean(axis=1))
+    raise ValueError(aggregate)
