@@ -105,6 +105,36 @@ int kvp_future_attn_mass(const void* q, const void* k, const float* lse, int dty
                          kvp_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * A2'. KVpop's supervision target (per-query-head future mass and its epilogue).
+ *
+ * KVpop, "Defining Future Attention Utility" (count normalisation N_t =
+ * max(1, S - (t + w)), the mean m_g(t) = F_g(t) / N_t of every query head g,
+ * log(eps + m) and the max over the heads that share a KV head; worked example
+ * N_t = 2, means 0.25 / 0.10, target -1.386) and "Alternative Aggregation
+ * Methods" (the probability-space mean over the group):
+ *
+ *   F_g[b, h*G+g, t] = sum_{i = t + window}^{seq_len - 1}
+ *                      exp(sm_scale * q[b, h*G+g, i] . k[b, h, t] - lse[b, h*G+g, i])
+ *   KVP_TARGET_MAX_LOG:   target[b, h, t] = max_g log(eps + F_g / N_t)
+ *   KVP_TARGET_MEAN_PROB: target[b, h, t] = log(eps + (1/G) sum_g F_g / N_t)
+ *
+ * Inputs as in kvp_future_attn_mass.  Outputs (each nullable, at least one):
+ * target [n_batch, h_kv, seq_len] float32; F_heads [n_batch, h_q, seq_len]
+ * float32 (the per-query-head mass); F [n_batch, h_kv, seq_len] float32 (their
+ * group sum).  eps >= 0 (eps = 0 gives -inf where a key receives no mass);
+ * sm_scale > 0.  workspace: at least kvp_future_attn_target_workspace_size()
+ * bytes, 256-byte aligned.
+ * ------------------------------------------------------------------------- */
+#define KVP_TARGET_MAX_LOG 0
+#define KVP_TARGET_MEAN_PROB 1
+size_t kvp_future_attn_target_workspace_size(int dtype, int n_batch, int h_q, int h_kv,
+                                             int seq_len, int head_dim, int window);
+int kvp_future_attn_target(const void* q, const void* k, const float* lse, int dtype, int n_batch,
+                           int h_q, int h_kv, int seq_len, int head_dim, float sm_scale,
+                           int window, float eps, int aggregate, float* target, float* F_heads,
+                           float* F, void* workspace, size_t workspace_bytes, kvp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * A0. Head-wise budgets from the closed-form Soft-TopK.
  *
  * LKV: End-to-End Learning of Head-wise Budgets and Token Selection for LLM

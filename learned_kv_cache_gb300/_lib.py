@@ -28,6 +28,9 @@ SIGNATURES = {
     "kvp_lse_pass": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P]),
     "kvp_future_attn_mass_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "kvp_future_attn_mass": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _SZ, _P]),
+    "kvp_future_attn_target_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "kvp_future_attn_target": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _F, _I, _P, _P, _P, _P,
+                                    _SZ, _P]),
     "kvp_soft_topk_budgets": (_I, [_P, _I, _D, _I, _P, _P, _P]),
     "kvp_select_topk": (_I, [_P, _I, _I, _I64, _P, _I, _I, _P, _I, _P, _P]),
     "kvp_compact_kv": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P]),
@@ -165,6 +168,41 @@ def kvp_future_attn_mass(q, k, lse, window, sm_scale=None, F=None, workspace=Non
                                      ws_bytes, _stream(stream))
     _check("kvp_future_attn_mass", rc)
     return F[0] if squeeze and F.dim() == 3 else F
+
+
+KVP_TARGET_MAX_LOG, KVP_TARGET_MEAN_PROB = 0, 1
+
+
+def kvp_future_attn_target(q, k, lse, window, eps=0.0, aggregate="max_log", sm_scale=None,
+                           target=None, F_heads=None, F=None, want=("target",), workspace=None,
+                           stream=None):
+    """KVpop target: returns (target [B,H_kv,S], F_heads [B,H_q,S] or None, F [B,H_kv,S] or None)."""
+    q4, k4 = _bhsd(q, k)
+    B, Hq, S, D = q4.shape
+    Hkv = k4.shape[1]
+    _need(q4, "q")
+    _need(k4, "k", dtype=q4.dtype, shape=(B, Hkv, S, D))
+    _need(lse, "lse", torch.float32)
+    if sm_scale is None:
+        sm_scale = D ** -0.5
+    agg = {"max_log": KVP_TARGET_MAX_LOG, "mean_prob": KVP_TARGET_MEAN_PROB}[aggregate]
+    dev = q.device
+    if target is None and "target" in want:
+        target = torch.empty(B, Hkv, S, device=dev, dtype=torch.float32)
+    if F_heads is None and "F_heads" in want:
+        F_heads = torch.empty(B, Hq, S, device=dev, dtype=torch.float32)
+    if F is None and "F" in want:
+        F = torch.empty(B, Hkv, S, device=dev, dtype=torch.float32)
+    need = int(load().kvp_future_attn_target_workspace_size(_dtype(q4), B, Hq, Hkv, S, D, int(window)))
+    if workspace is None:
+        workspace = torch.empty(need, device=dev, dtype=torch.uint8)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    rc = load().kvp_future_attn_target(_ptr(q4), _ptr(k4), _ptr(lse), _dtype(q4), B, Hq, Hkv, S, D,
+                                       float(sm_scale), int(window), float(eps), agg, _ptr(target),
+                                       _ptr(F_heads), _ptr(F), _ptr(workspace), ws_bytes,
+                                       _stream(stream))
+    _check("kvp_future_attn_target", rc)
+    return target, F_heads, F
 
 
 def kvp_soft_topk_budgets(scores, k, t, ratios=None, budgets=None, stream=None):

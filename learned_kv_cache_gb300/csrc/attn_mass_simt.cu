@@ -125,12 +125,13 @@ __global__ void __launch_bounds__(256) lse_simt_kernel(const T* __restrict__ q,
   }
 }
 
+// per_head = 0: F[b, h, j] (group sum); per_head = 1: F[b, h*G+g, j] per query head.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) fam_simt_kernel(const T* __restrict__ q,
                                                        const T* __restrict__ k,
                                                        const float* __restrict__ lse, int Hq,
                                                        int Hkv, int S, float c2, int w,
-                                                       float* __restrict__ F) {
+                                                       float* __restrict__ F, int per_head) {
   extern __shared__ float sm[];
   float* As = sm;
   float* Bs = sm + D * LD;
@@ -167,13 +168,55 @@ __global__ void __launch_bounds__(256) fam_simt_kernel(const T* __restrict__ q,
           }
         }
       }
+      if (per_head) {
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const float tot = row_sum16(f[a]);
+          const int j = j0 + ty * 4 + a;
+          if (tx == 0 && j < S) F[(size_t)(b * Hq + hq) * S + j] = tot;
+          f[a] = 0.f;
+        }
+      }
     }
+  }
+  if (per_head) {
+    if (first >= S) {                        // no future queries: every head's mass is 0
+      for (int e = threadIdx.x; e < G * TM; e += blockDim.x) {
+        const int g = e / TM, j = j0 + e % TM;
+        if (j < S) F[(size_t)(b * Hq + hk * G + g) * S + j] = 0.f;
+      }
+    }
+    return;
   }
 #pragma unroll
   for (int a = 0; a < 4; ++a) {
     const float tot = row_sum16(f[a]);
     const int j = j0 + ty * 4 + a;
     if (tx == 0 && j < S) F[(size_t)(b * Hkv + hk) * S + j] = tot;
+  }
+}
+
+// KVpop target (KVpop, "Defining Future Attention Utility" and "Alternative Aggregation
+// Methods"): N_t = max(1, S - (t + w)), m_g = F_g / N_t, and per KV head either
+// max_g log(eps + m_g) or log(eps + mean_g m_g); also the raw group sum of F_g.
+__global__ void target_epilogue_kernel(const float* __restrict__ Fh, int Hq, int Hkv, int S, int w,
+                                       float eps, int aggregate, float* __restrict__ target,
+                                       float* __restrict__ F, long long total) {
+  const int G = Hq / Hkv;
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (long long)gridDim.x * blockDim.x) {
+    const int j = (int)(e % S);
+    const long long bh = e / S;                 // b * Hkv + h
+    const int b = (int)(bh / Hkv), h = (int)(bh % Hkv);
+    const float N = (float)max(1, S - (j + w));
+    float sum = 0.f, best = -INFINITY;
+    for (int g = 0; g < G; ++g) {
+      const float fg = Fh[((size_t)b * Hq + h * G + g) * S + j];
+      sum += fg;
+      best = fmaxf(best, logf(eps + fg / N));
+    }
+    if (target) target[e] = aggregate == 0 ? best : logf(eps + sum / (N * (float)G));
+    if (F) F[e] = sum;
   }
 }
 
@@ -192,14 +235,14 @@ cudaError_t lse_simt(const void* q, const void* k, AttnShape s, float scale, flo
 
 template <typename T, int D>
 cudaError_t fam_simt(const void* q, const void* k, const float* lse, AttnShape s, float scale,
-                     int w, float* F, cudaStream_t st) {
+                     int w, float* F, cudaStream_t st, int per_head) {
   const size_t smem = (2 * D * LD + TN) * sizeof(float);
   auto kern = fam_simt_kernel<T, D>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   dim3 grid((s.seq_len + TM - 1) / TM, s.h_kv, s.n_batch);
   count_launches(1);
   kern<<<grid, 256, smem, st>>>((const T*)q, (const T*)k, lse, s.h_q, s.h_kv, s.seq_len,
-                                scale * KVP_LOG2E, w, F);
+                                scale * KVP_LOG2E, w, F, per_head);
   return cudaGetLastError();
 }
 
@@ -219,16 +262,28 @@ cudaError_t launch_lse_simt(const void* q, const void* k, int dtype, AttnShape s
 }
 
 cudaError_t launch_fam_simt(const void* q, const void* k, const float* lse, int dtype, AttnShape s,
-                            float scale, int w, float* F, cudaStream_t st) {
+                            float scale, int w, float* F, cudaStream_t st, int per_head) {
   const bool d128 = s.head_dim == 128;
   switch (dtype) {
-    case KVP_F32: return d128 ? fam_simt<float, 128>(q, k, lse, s, scale, w, F, st)
-                              : fam_simt<float, 64>(q, k, lse, s, scale, w, F, st);
-    case KVP_BF16: return d128 ? fam_simt<__nv_bfloat16, 128>(q, k, lse, s, scale, w, F, st)
-                               : fam_simt<__nv_bfloat16, 64>(q, k, lse, s, scale, w, F, st);
-    default: return d128 ? fam_simt<__half, 128>(q, k, lse, s, scale, w, F, st)
-                         : fam_simt<__half, 64>(q, k, lse, s, scale, w, F, st);
+    case KVP_F32: return d128 ? fam_simt<float, 128>(q, k, lse, s, scale, w, F, st, per_head)
+                              : fam_simt<float, 64>(q, k, lse, s, scale, w, F, st, per_head);
+    case KVP_BF16: return d128 ? fam_simt<__nv_bfloat16, 128>(q, k, lse, s, scale, w, F, st, per_head)
+                               : fam_simt<__nv_bfloat16, 64>(q, k, lse, s, scale, w, F, st, per_head);
+    default: return d128 ? fam_simt<__half, 128>(q, k, lse, s, scale, w, F, st, per_head)
+                         : fam_simt<__half, 64>(q, k, lse, s, scale, w, F, st, per_head);
   }
+}
+
+cudaError_t launch_target_epilogue(const float* F_heads, int n_batch, int h_q, int h_kv, int S,
+                                   int window, float eps, int aggregate, float* target, float* F,
+                                   cudaStream_t st) {
+  const long long total = (long long)n_batch * h_kv * S;
+  long long blocks = (total + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  count_launches(1);
+  target_epilogue_kernel<<<(unsigned)blocks, 256, 0, st>>>(F_heads, h_q, h_kv, S, window, eps, aggregate,
+                                                           target, F, total);
+  return cudaGetLastError();
 }
 
 }  // namespace kvp

@@ -94,6 +94,7 @@ struct TcParams {
   int n_groups;          // LSE pass: B*Hq; mass pass: B*Hkv
   int NQT;               // LSE pass: query tiles per head
   int NT0, TPC, CMAX, NKT, Nf;   // mass pass schedule
+  int per_head;          // mass pass: keep each query head's sum (partials [.., G, 2 halves, 128])
   int* status;
 };
 
@@ -426,6 +427,16 @@ __global__ void __launch_bounds__(THREADS, 2)
           acc01 = fadd2(acc01, pack2(fast_exp2(x0), fast_exp2(x1)));
           acc23 = fadd2(acc23, pack2(fast_exp2(x2), fast_exp2(x3)));
         }
+        if (p.per_head && u == it.per_head - 1) {   // last tile of this query head in the item
+          float f0, f1, f2, f3;
+          unpack2(acc01, f0, f1);
+          unpack2(acc23, f2, f3);
+          const int gh = t / it.per_head;
+          float* dst = p.out + ((((size_t)it.group * p.NKT + it.tile) * p.CMAX + it.chunk) * p.G + gh) * 2 * BM;
+          dst[half * BM + r] = (f0 + f1) + (f2 + f3);
+          acc01 = 0;
+          acc23 = 0;
+        }
         __syncwarp();
       }
     }
@@ -446,7 +457,7 @@ __global__ void __launch_bounds__(THREADS, 2)
         const int i = it.tile * BM + r;
         if (i < p.S) p.out[(size_t)it.group * p.S + i] = (M + __log2f(L)) * KVP_LN2;
       }
-    } else {
+    } else if (!p.per_head) {
       float f0, f1, f2, f3;
       unpack2(acc01, f0, f1);
       unpack2(acc23, f2, f3);
@@ -480,6 +491,25 @@ __global__ void __launch_bounds__(BM) fam_reduce_kernel(const float* __restrict_
   float f = 0.f;
   for (int c = 0; c < nch; ++c) f += src[(size_t)c * BM];
   F[(size_t)group * S + j] = f;
+}
+
+// F_heads[b, h*G + g, j] = sum over the chunks (and both column halves) of key tile j/128 of
+// query head g's partial sums, in chunk order.
+__global__ void __launch_bounds__(BM) fam_reduce_heads_kernel(const float* __restrict__ part, int S, int Hkv,
+                                                              int G, int NT0, int TPC, int CMAX, int NKT,
+                                                              float* __restrict__ F_heads) {
+  const int jt = blockIdx.x, group = blockIdx.y, r = threadIdx.x;
+  const int j = jt * BM + r;
+  if (j >= S) return;
+  const int nt = max(0, NT0 - jt);
+  const int nch = (nt + TPC - 1) / TPC;
+  const int b = group / Hkv, h = group % Hkv;
+  for (int g = 0; g < G; ++g) {
+    const float* src = part + (((size_t)group * NKT + jt) * CMAX * G + g) * 2 * BM + r;
+    float f = 0.f;
+    for (int c = 0; c < nch; ++c) f += src[(size_t)c * G * 2 * BM] + src[(size_t)c * G * 2 * BM + BM];
+    F_heads[((size_t)b * Hkv * G + h * G + g) * S + j] = f;
+  }
 }
 
 // ---------------------------------------------------------------- host side
@@ -561,9 +591,10 @@ bool tc_supported(int dtype, AttnShape s) {
   return (dtype == KVP_BF16 || dtype == KVP_F16) && s.head_dim == HD && encode_fn() != nullptr;
 }
 
-size_t fam_tc_workspace_size(AttnShape s, int window) {
+size_t fam_tc_workspace_size(AttnShape s, int window, int per_head) {
   const FamSched f = fam_schedule(s, window);
-  return (size_t)s.n_batch * s.h_kv * f.NKT * f.CMAX * BM * sizeof(float);
+  const size_t heads = per_head ? (size_t)2 * (s.h_q / s.h_kv) : 1;
+  return (size_t)s.n_batch * s.h_kv * f.NKT * f.CMAX * heads * BM * sizeof(float);
 }
 
 cudaError_t launch_lse_tc(const void* q, const void* k, int dtype, AttnShape s, float scale,
@@ -587,9 +618,9 @@ cudaError_t launch_lse_tc(const void* q, const void* k, int dtype, AttnShape s, 
 
 cudaError_t launch_fam_tc(const void* q, const void* k, const float* lse, int dtype, AttnShape s,
                           float scale, int window, float* F, void* ws, size_t ws_bytes, int* status,
-                          cudaStream_t st) {
+                          cudaStream_t st, int per_head) {
   const FamSched f = fam_schedule(s, window);
-  if (ws_bytes < fam_tc_workspace_size(s, window)) return cudaErrorInvalidValue;
+  if (ws_bytes < fam_tc_workspace_size(s, window, per_head)) return cudaErrorInvalidValue;
   TcParams p{};
   p.S = s.seq_len;
   p.Hq = s.h_q;
@@ -606,6 +637,7 @@ cudaError_t launch_fam_tc(const void* q, const void* k, const float* lse, int dt
   p.CMAX = f.CMAX;
   p.NKT = f.NKT;
   p.Nf = f.Nf;
+  p.per_head = per_head;
   p.status = status;
   const long long items = (long long)(f.Nf + f.Np) * p.n_groups;
   if (items > 0) {
@@ -618,8 +650,12 @@ cudaError_t launch_fam_tc(const void* q, const void* k, const float* lse, int dt
     if (e != cudaSuccess) return e;
   }
   count_launches(1);
-  fam_reduce_kernel<<<dim3(f.NKT, p.n_groups), BM, 0, st>>>((const float*)ws, s.seq_len, f.NT0, f.TPC,
-                                                            f.CMAX, f.NKT, F);
+  if (per_head)
+    fam_reduce_heads_kernel<<<dim3(f.NKT, p.n_groups), BM, 0, st>>>((const float*)ws, s.seq_len, s.h_kv, p.G,
+                                                                    f.NT0, f.TPC, f.CMAX, f.NKT, F);
+  else
+    fam_reduce_kernel<<<dim3(f.NKT, p.n_groups), BM, 0, st>>>((const float*)ws, s.seq_len, f.NT0, f.TPC,
+                                                              f.CMAX, f.NKT, F);
   return cudaGetLastError();
 }
 

@@ -183,6 +183,59 @@ int kvp_future_attn_mass(const void* q, const void* k, const float* lse, int dty
   return KVP_OK;
 }
 
+static size_t target_heads_bytes(int n_batch, int h_q, int seq_len) {
+  return (((size_t)n_batch * h_q * seq_len * sizeof(float)) + 255) & ~(size_t)255;
+}
+
+size_t kvp_future_attn_target_workspace_size(int dtype, int n_batch, int h_q, int h_kv, int seq_len,
+                                             int head_dim, int window) {
+  if (check_dtype(dtype) != KVP_OK || check_attn_shape(n_batch, h_q, h_kv, seq_len, head_dim) != KVP_OK ||
+      window < 0)
+    return 0;
+  kvp::AttnShape s{n_batch, h_q, h_kv, seq_len, head_dim};
+  const size_t part = kvp::tc_supported(dtype, s) ? kvp::fam_tc_workspace_size(s, window, 1) : 0;
+  return target_heads_bytes(n_batch, h_q, seq_len) + part;
+}
+
+int kvp_future_attn_target(const void* q, const void* k, const float* lse, int dtype, int n_batch,
+                           int h_q, int h_kv, int seq_len, int head_dim, float sm_scale, int window,
+                           float eps, int aggregate, float* target, float* F_heads, float* F,
+                           void* workspace, size_t workspace_bytes, kvp_stream_t stream) {
+  g_last_error.clear();
+  KVP_TRY(check_dtype(dtype));
+  KVP_TRY(check_attn_shape(n_batch, h_q, h_kv, seq_len, head_dim));
+  if (!q || !k || !lse) return fail(KVP_ERR_INVALID_ARG, "null q/k/lse");
+  if (!target && !F_heads && !F) return fail(KVP_ERR_INVALID_ARG, "no output requested");
+  if (!aligned16(q) || !aligned16(k)) return fail(KVP_ERR_INVALID_ARG, "q/k not 16-byte aligned");
+  if (window < 0) return fail(KVP_ERR_INVALID_ARG, "window=%d < 0", window);
+  if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return fail(KVP_ERR_INVALID_ARG, "sm_scale must be > 0");
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(KVP_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if (aggregate != KVP_TARGET_MAX_LOG && aggregate != KVP_TARGET_MEAN_PROB)
+    return fail(KVP_ERR_INVALID_ARG, "aggregate=%d", aggregate);
+  const size_t need = kvp_future_attn_target_workspace_size(dtype, n_batch, h_q, h_kv, seq_len, head_dim, window);
+  if (!workspace || workspace_bytes < need)
+    return fail(KVP_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+  if (((uintptr_t)workspace & 255u) != 0) return fail(KVP_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+  int* st = nullptr;
+  KVP_TRY(status_ptr(&st));
+  kvp::AttnShape s{n_batch, h_q, h_kv, seq_len, head_dim};
+  float* heads = F_heads ? F_heads : (float*)workspace;
+  char* part = (char*)workspace + target_heads_bytes(n_batch, h_q, seq_len);
+  cudaError_t e = kvp::tc_supported(dtype, s)
+                      ? kvp::launch_fam_tc(q, k, lse, dtype, s, sm_scale, window, heads, part,
+                                           workspace_bytes - target_heads_bytes(n_batch, h_q, seq_len), st,
+                                           (cudaStream_t)stream, 1)
+                      : kvp::launch_fam_simt(q, k, lse, dtype, s, sm_scale, window, heads,
+                                             (cudaStream_t)stream, 1);
+  if (e != cudaSuccess) return cuda_fail(e, "kvp_future_attn_target launch");
+  if (target || F) {
+    e = kvp::launch_target_epilogue(heads, n_batch, h_q, h_kv, seq_len, window, eps, aggregate, target, F,
+                                    (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kvp_future_attn_target epilogue");
+  }
+  return KVP_OK;
+}
+
 int kvp_soft_topk_budgets(const double* scores, int n, double k, int t, double* ratios,
                           int32_t* budgets, kvp_stream_t stream) {
   g_last_error.clear();

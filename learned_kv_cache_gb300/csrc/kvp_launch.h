@@ -19,16 +19,21 @@ struct AttnShape {
 cudaError_t launch_lse_simt(const void* q, const void* k, int dtype, AttnShape s, float scale,
                             float* lse, cudaStream_t st);
 cudaError_t launch_fam_simt(const void* q, const void* k, const float* lse, int dtype, AttnShape s,
-                            float scale, int window, float* F, cudaStream_t st);
+                            float scale, int window, float* F, cudaStream_t st, int per_head = 0);
+// KVpop target from per-query-head mass: count normalisation, log(eps + m), group max / mean.
+cudaError_t launch_target_epilogue(const float* F_heads, int n_batch, int h_q, int h_kv, int S,
+                                   int window, float eps, int aggregate, float* target, float* F,
+                                   cudaStream_t st);
 
 // tcgen05 / TMA passes (bf16 / f16, head_dim 128).
 bool tc_supported(int dtype, AttnShape s);
-size_t fam_tc_workspace_size(AttnShape s, int window);
+size_t fam_tc_workspace_size(AttnShape s, int window, int per_head = 0);
 cudaError_t launch_lse_tc(const void* q, const void* k, int dtype, AttnShape s, float scale,
                           float* lse, int* status, cudaStream_t st);
+// per_head = 1: F receives each query head's mass, [n_batch, h_q, seq_len].
 cudaError_t launch_fam_tc(const void* q, const void* k, const float* lse, int dtype, AttnShape s,
                           float scale, int window, float* F, void* ws, size_t ws_bytes,
-                          int* status, cudaStream_t st);
+                          int* status, cudaStream_t st, int per_head = 0);
 
 cudaError_t launch_soft_topk(const double* x, int n, double k, int t, double* ratios,
                              int32_t* budgets, cudaStream_t st);
