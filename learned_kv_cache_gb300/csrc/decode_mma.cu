@@ -47,9 +47,13 @@ struct Dm {
   static constexpr int KSTEPS = D / 16;
   static constexpr int PSTRIDE = 2 * DM_QPAD + DM_QPAD * D; // partial: m[8], l[8], o[8][D]
   static constexpr int OFF_BAR = STAGES * STAGE_BYTES;
-  static constexpr int OFF_SM = OFF_BAR + 128;              // merge scratch
+  // Merge scratch of the four consumer warps.  It aliases the stage ring: every CTA's tile
+  // range lies in one row (see decode_mma_plan), so the merge runs only after the last tile
+  // has been consumed and no copy is in flight.
+  static constexpr int OFF_SM = 0;
   static constexpr int SCRATCH = (2 * DM_CWARPS * DM_QPAD + DM_CWARPS * DM_QPAD * D) * 4;
-  static constexpr int OFF_CST = OFF_SM + SCRATCH;          // merged state of this CTA
+  static_assert(SCRATCH <= STAGES * STAGE_BYTES, "merge scratch must fit in the stage ring");
+  static constexpr int OFF_CST = OFF_BAR + 128;             // merged state of this CTA
   static constexpr int OFF_FLAG = OFF_CST + PSTRIDE * 4;
   static constexpr int MAXC = (DM_CWARPS * DM_QPAD * D) / (2 + 2 * DM_QPAD);   // combine capacity
   static constexpr int SMEM = OFF_FLAG + 16 + 1024;         // + alignment slack
@@ -238,6 +242,9 @@ __global__ void __launch_bounds__(DM_THREADS, 2)
     // row merges all partials and writes the output.
     auto finish_row = [&](int r) {
       const int ctid = threadIdx.x;          // 0..127
+      // every consumer warp is done with the stage ring before the scratch (which aliases it)
+      // is written
+      asm volatile("bar.sync 1, %0;" ::"r"(DM_CWARPS * 32));
       float l0 = ls[0], l1 = ls[1];
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) {
