@@ -192,6 +192,33 @@ int kvp_compact_kv(const void* k, const void* v, int dtype, int R, int T, int he
                    void* v_out, kvp_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * A4'. In-place eviction of a static (ring) decode cache.
+ *
+ * How much KV cache can you prune, "What we did" (attention-score policy: keep
+ * the first tokens, always keep the newest ones, fill the rest with the tokens
+ * that received the most attention) and "Conclusion" (a ring or static cache
+ * overwrites old entries in place instead of copying the kept ones).
+ *
+ * Per row r of a cache with `cap` slots: if fill[r] < cap the new token is
+ * appended at slot fill[r] and fill[r] grows by one; otherwise the slot with the
+ * lowest slot_score among the slots whose token position p satisfies
+ * n_sink <= p <= new_pos - n_recent is overwritten (NaN first, -0.0 == +0.0,
+ * ties to the newer token).  The chosen slot receives new_k / new_v, position
+ * new_pos and score 0; out_slot[r] (nullable) reports it.
+ *
+ * kc, vc [R, cap, head_dim] dtype (updated in place); slot_pos [R, cap] int32;
+ * slot_score [R, cap] float32 (the cumulative attention each slot's token has
+ * received, e.g. accumulated by kvp_decode_attn's key mass with key_pos NULL);
+ * fill [R] int32; new_k, new_v [R, head_dim] dtype.  Requires
+ * cap >= n_sink + n_recent and n_recent >= 1 (then a full cache always has a
+ * slot to give up); positions in a full row must be distinct, else
+ * KVP_ERR_DEVICE_CHECK.
+ * ------------------------------------------------------------------------- */
+int kvp_ring_insert(void* kc, void* vc, int32_t* slot_pos, float* slot_score, int32_t* fill,
+                    int dtype, int R, int cap, int head_dim, const void* new_k, const void* new_v,
+                    int new_pos, int n_sink, int n_recent, int32_t* out_slot, kvp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * A5. Single-token decode attention over a (pruned) cache, split along keys.
  *
  * How much KV cache can you prune, "What we did" and "Bounded windows"

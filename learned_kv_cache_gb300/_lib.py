@@ -34,6 +34,7 @@ SIGNATURES = {
     "kvp_soft_topk_budgets": (_I, [_P, _I, _D, _I, _P, _P, _P]),
     "kvp_select_topk": (_I, [_P, _I, _I, _I64, _P, _I, _I, _P, _I, _P, _P]),
     "kvp_compact_kv": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P]),
+    "kvp_ring_insert": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _I, _I, _P, _P]),
     "kvp_decode_attn_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "kvp_decode_attn": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _F, _P, _P, _P, _I, _I, _P,
                              _SZ, _P]),
@@ -261,6 +262,26 @@ def kvp_compact_kv(k, v, idx, count, k_out=None, v_out=None, stream=None):
                                _ptr(k_out), _ptr(v_out), _stream(stream))
     _check("kvp_compact_kv", rc)
     return k_out, v_out
+
+
+def kvp_ring_insert(kc, vc, slot_pos, slot_score, fill, new_k, new_v, new_pos, n_sink, n_recent,
+                    out_slot=None, stream=None):
+    """Insert one new token per row into a static cache [R, cap, D] in place (see kvp.h)."""
+    _need(kc, "kc")
+    R, cap, D = kc.shape
+    _need(vc, "vc", kc.dtype, (R, cap, D))
+    _need(slot_pos, "slot_pos", torch.int32, (R, cap))
+    _need(slot_score, "slot_score", torch.float32, (R, cap))
+    _need(fill, "fill", torch.int32, (R,))
+    _need(new_k, "new_k", kc.dtype, (R, D))
+    _need(new_v, "new_v", kc.dtype, (R, D))
+    if out_slot is not None:
+        _need(out_slot, "out_slot", torch.int32, (R,))
+    rc = load().kvp_ring_insert(_ptr(kc), _ptr(vc), _ptr(slot_pos), _ptr(slot_score), _ptr(fill),
+                                _dtype(kc), R, cap, D, _ptr(new_k), _ptr(new_v), int(new_pos),
+                                int(n_sink), int(n_recent), _ptr(out_slot), _stream(stream))
+    _check("kvp_ring_insert", rc)
+    return out_slot
 
 
 def kvp_decode_attn_workspace_size(n_layers, h_q, h_kv, head_dim, T_cap, with_key_mass):

@@ -284,6 +284,31 @@ int kvp_compact_kv(const void* k, const void* v, int dtype, int R, int T, int he
   return KVP_OK;
 }
 
+int kvp_ring_insert(void* kc, void* vc, int32_t* slot_pos, float* slot_score, int32_t* fill,
+                    int dtype, int R, int cap, int head_dim, const void* new_k, const void* new_v,
+                    int new_pos, int n_sink, int n_recent, int32_t* out_slot, kvp_stream_t stream) {
+  g_last_error.clear();
+  KVP_TRY(check_dtype(dtype));
+  if (!kc || !vc || !slot_pos || !slot_score || !fill || !new_k || !new_v)
+    return fail(KVP_ERR_INVALID_ARG, "null pointer");
+  if (R < 1 || cap < 1) return fail(KVP_ERR_INVALID_ARG, "R=%d cap=%d must be >= 1", R, cap);
+  if (head_dim != 64 && head_dim != 128) return fail(KVP_ERR_UNSUPPORTED, "head_dim=%d", head_dim);
+  if (n_sink < 0 || n_recent < 1) return fail(KVP_ERR_INVALID_ARG, "need n_sink >= 0 and n_recent >= 1");
+  if (cap < n_sink + n_recent)
+    return fail(KVP_ERR_INVALID_ARG, "cap=%d < n_sink + n_recent = %d: a full cache would have nothing to evict",
+                cap, n_sink + n_recent);
+  if (new_pos < 0) return fail(KVP_ERR_INVALID_ARG, "new_pos=%d < 0", new_pos);
+  if (!aligned16(kc) || !aligned16(vc) || !aligned16(new_k) || !aligned16(new_v))
+    return fail(KVP_ERR_INVALID_ARG, "kc/vc/new_k/new_v not 16-byte aligned");
+  int* st = nullptr;
+  KVP_TRY(status_ptr(&st));
+  cudaError_t e = kvp::launch_ring_insert(kc, vc, slot_pos, slot_score, fill, R, cap, head_dim * elem_size(dtype),
+                                          new_k, new_v, new_pos, n_sink, n_recent, out_slot, st,
+                                          (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kvp_ring_insert launch");
+  return KVP_OK;
+}
+
 size_t kvp_decode_attn_workspace_size(int n_layers, int h_q, int h_kv, int head_dim, int T_cap,
                                       int with_key_mass) {
   if (n_layers < 1 || h_q < 1 || h_kv < 1 || h_q % h_kv || T_cap < 1 ||

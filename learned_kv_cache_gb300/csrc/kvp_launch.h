@@ -44,6 +44,11 @@ cudaError_t launch_compact(const void* k, const void* v, int row_bytes, int R, i
                            const int32_t* idx, const int32_t* count, int b_max, void* k_out,
                            void* v_out, int* status, cudaStream_t st);
 
+cudaError_t launch_ring_insert(void* kc, void* vc, int32_t* slot_pos, float* slot_score, int32_t* fill,
+                               int R, int cap, int row_bytes, const void* new_k, const void* new_v,
+                               int new_pos, int n_sink, int n_recent, int32_t* out_slot, int* status,
+                               cudaStream_t st);
+
 struct DecodePlan {
   int R, G;
   // fp32 cache path (grid of key chunks x rows)
