@@ -333,6 +333,12 @@ def run_kvp(args):
     # pruned-cache decode on the decode-eviction workload (HBM bound)
     decode = decode_eviction_measure(kvp, dev, K, args.warmup, flush, peaks, ws)
 
+    # NEXT rows: KVpop target epilogue and the steady-state ring-cache decode step
+    next_rows = {
+        "kvpop_target": target_measure(kvp, x, plan, w, K, args.warmup, flush, peak, stream, dev),
+        "ring_decode_step": ring_step_measure(kvp, dev, K, args.warmup, flush, peaks),
+    }
+
     # end to end through the public API with host buffers
     e2e = e2e_measure(kvp, x, plan, budgets, w, K, args.warmup, stream, flops, ws, dev)
 
@@ -356,6 +362,7 @@ def run_kvp(args):
         "stages_ms": stage_mean,
         "roofline": roofline,
         "decode": decode,
+        "next_rows": next_rows,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": int(launches),
@@ -444,6 +451,97 @@ def decode_eviction_measure(kvp, dev, K, W, flush, peaks, ws):
     }
 
 
+def target_measure(kvp, x, plan, w, K, W, flush, peak, stream, dev):
+    """KVpop target on the same layer: per-query-head future mass through the tensor-core pass
+    plus the count-normalise / log / group-max epilogue, timed alone with L2 flushed."""
+    R, S = w.h_q, w.seq_len
+    tgt = torch.empty(1, w.h_kv, S, device=dev)
+    ws = torch.empty(kvp.kvp_future_attn_target_workspace_size(x["q"].dtype, 1, w.h_q, w.h_kv, S,
+                                                               w.head_dim, w.window),
+                     dtype=torch.uint8, device=dev)
+
+    def run():
+        kvp.kvp_future_attn_target(x["q"], x["k"], plan.lse, w.window, target=tgt,
+                                   want=("target",), workspace=ws)
+
+    for _ in range(W):
+        run()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    for e0, e1 in evs:
+        flush()
+        e0.record(stream)
+        run()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    kvp.kvp_check_device_status()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / K
+    ww = S - w.window
+    flops = 2.0 * w.head_dim * R * (ww * (ww + 1) // 2)
+    tf = flops / (ms / 1e3) / 1e12
+    return {"metric": "KVpop target pass TFLOP/s", "value": tf, "unit": "TFLOP/s",
+            "frac": tf / peak, "ms": ms, "flops": flops, "aggregate": "max_log",
+            "l2": "flushed before every launch"}
+
+
+def ring_step_measure(kvp, dev, K, W, flush, peaks, cap=4096):
+    """Steady-state decode with a static cache of `cap` slots per row on the Qwen2.5-1.5B decode
+    workload: per token, insert the new key/value in place (evicting the lowest accumulated
+    score outside sinks and the recent window) and decode over the cache while accumulating
+    each slot's attention.  L2 is flushed before every token step."""
+    w = kvp_inputs.QWEN25_15B_DECODE
+    x = kvp_inputs.make_decode_cache(w, device=dev)
+    R, T, D = w.rows, w.seq_len, w.head_dim
+    kc = x["k"][:, :cap].contiguous()
+    vc = x["v"][:, :cap].contiguous()
+    del x["k"], x["v"]
+    pos = torch.arange(cap, dtype=torch.int32, device=dev).repeat(R, 1).contiguous()
+    score = torch.rand(R, cap, generator=torch.Generator(device=dev).manual_seed(5), device=dev)
+    fill = torch.full((R,), cap, dtype=torch.int32, device=dev)
+    g = torch.Generator(device=dev).manual_seed(6)
+    steps = W + K
+    new_k = torch.randn(steps, R, D, generator=g, device=dev).to(kc.dtype)
+    new_v = torch.randn(steps, R, D, generator=g, device=dev).to(kc.dtype)
+    out = torch.empty(w.n_layers, w.h_q, D, device=dev)
+    slot = torch.empty(R, dtype=torch.int32, device=dev)
+    ws = torch.empty(kvp.kvp_decode_attn_workspace_size(w.n_layers, w.h_q, w.h_kv, D, cap, True),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(t):
+        kvp.kvp_ring_insert(kc, vc, pos, score, fill, new_k[t], new_v[t], cap + t, w.n_sink,
+                            w.n_recent, out_slot=slot)
+        kvp.kvp_decode_attn(x["q"], kc, vc, fill, out=out, key_mass=score, accumulate=True,
+                            workspace=ws)
+
+    for t in range(W):
+        step(t)
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    for i, e in enumerate(evs):
+        flush()
+        e[0].record(stream)
+        kvp.kvp_ring_insert(kc, vc, pos, score, fill, new_k[W + i], new_v[W + i], cap + W + i,
+                            w.n_sink, w.n_recent, out_slot=slot)
+        e[1].record(stream)
+        kvp.kvp_decode_attn(x["q"], kc, vc, fill, out=out, key_mass=score, accumulate=True,
+                            workspace=ws)
+        e[2].record(stream)
+    torch.cuda.synchronize(dev)
+    kvp.kvp_check_device_status()
+    t_ins = sum(e[0].elapsed_time(e[1]) for e in evs) / K
+    t_dec = sum(e[1].elapsed_time(e[2]) for e in evs) / K
+    elt = kc.element_size()
+    ins_bytes = R * cap * 8 + 2 * R * D * elt * 2
+    dec_bytes = 2 * R * cap * D * elt + x["q"].numel() * elt + out.numel() * 4 + R * cap * 8
+    hbm = float(peaks["hbm_gbs"])
+    gbs = (ins_bytes + dec_bytes) / ((t_ins + t_dec) / 1e3) / 1e9
+    return {"metric": "ring-cache decode step HBM GB/s", "value": gbs, "unit": "GB/s",
+            "frac": gbs / hbm, "peak": hbm, "cap": cap, "us_per_token": (t_ins + t_dec) * 1e3,
+            "ring_insert_us": t_ins * 1e3, "decode_with_key_mass_us": t_dec * 1e3,
+            "bytes": ins_bytes + dec_bytes, "l2": "flushed before every token step"}
+
+
 def e2e_measure(kvp, x, plan, budgets, w, K, W, stream, flops, ws, dev):
     """Whole step through the public API from pinned host buffers: H2D of Q/K/V and the decode
     query, the five stages, D2H of F, the kept indices/counts and the decode output."""
@@ -488,8 +586,9 @@ def e2e_measure(kvp, x, plan, budgets, w, K, W, stream, flops, ws, dev):
 def run_ncu_case(args):
     """A fixed case for profiler captures: `--steps` launches of one stage, no timing.
     lse / fam: one Qwen3-4B-shaped layer at --seq-len (default 32768: Q = 256 MiB, larger than
-    L2); decode / select / compact: the Qwen2.5-1.5B decode-eviction shapes (T = 120000,
-    28 layers x 2 KV heads, budget 4096)."""
+    L2); decode / select / compact / ring: the Qwen2.5-1.5B decode-eviction shapes (T = 120000,
+    28 layers x 2 KV heads, budget 4096; ring: a full static cache of 4096 slots per row, one
+    insert plus one decode with accumulated key mass per step)."""
     import learned_kv_cache_gb300 as kvp
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -530,6 +629,18 @@ def run_ncu_case(args):
             cnt = torch.full((R,), b, dtype=torch.int32, device=dev)
             for _ in range(args.steps):
                 kvp.kvp_compact_kv(k, v, idx, cnt)
+        elif case == "ring":
+            # static cache of `b` slots per row, full: insert + decode with accumulated key mass
+            q = torch.randn(w.n_layers, w.h_q, D, generator=gen, device=dev).half()
+            kc = torch.randn(R, b, D, generator=gen, device=dev).half()
+            vc = torch.randn(R, b, D, generator=gen, device=dev).half()
+            pos = torch.arange(b, dtype=torch.int32, device=dev).repeat(R, 1).contiguous()
+            score = torch.rand(R, b, generator=gen, device=dev)
+            fill = torch.full((R,), b, dtype=torch.int32, device=dev)
+            nk = torch.randn(R, D, generator=gen, device=dev).half()
+            for t in range(args.steps):
+                kvp.kvp_ring_insert(kc, vc, pos, score, fill, nk, nk, b + t, w.n_sink, w.n_recent)
+                kvp.kvp_decode_attn(q, kc, vc, fill, key_mass=score, accumulate=True)
         else:
             raise SystemExit(f"unknown --ncu-case {case}")
     torch.cuda.synchronize(dev)

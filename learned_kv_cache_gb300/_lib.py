@@ -174,6 +174,12 @@ def kvp_future_attn_mass(q, k, lse, window, sm_scale=None, F=None, workspace=Non
 KVP_TARGET_MAX_LOG, KVP_TARGET_MEAN_PROB = 0, 1
 
 
+def kvp_future_attn_target_workspace_size(dtype, n_batch, h_q, h_kv, seq_len, head_dim, window):
+    dt = _DTYPE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return int(load().kvp_future_attn_target_workspace_size(dt, n_batch, h_q, h_kv, seq_len,
+                                                            head_dim, window))
+
+
 def kvp_future_attn_target(q, k, lse, window, eps=0.0, aggregate="max_log", sm_scale=None,
                            target=None, F_heads=None, F=None, want=("target",), workspace=None,
                            stream=None):
@@ -194,7 +200,7 @@ def kvp_future_attn_target(q, k, lse, window, eps=0.0, aggregate="max_log", sm_s
         F_heads = torch.empty(B, Hq, S, device=dev, dtype=torch.float32)
     if F is None and "F" in want:
         F = torch.empty(B, Hkv, S, device=dev, dtype=torch.float32)
-    need = int(load().kvp_future_attn_target_workspace_size(_dtype(q4), B, Hq, Hkv, S, D, int(window)))
+    need = kvp_future_attn_target_workspace_size(_dtype(q4), B, Hq, Hkv, S, D, int(window))
     if workspace is None:
         workspace = torch.empty(need, device=dev, dtype=torch.uint8)
     ws_bytes = workspace.numel() * workspace.element_size()

@@ -56,8 +56,12 @@ struct Dm {
   static constexpr int OFF_CST = OFF_BAR + 128;             // merged state of this CTA
   static constexpr int OFF_FLAG = OFF_CST + PSTRIDE * 4;
   static constexpr int MAXC = (DM_CWARPS * DM_QPAD * D) / (2 + 2 * DM_QPAD);   // combine capacity
-  static constexpr int SMEM = OFF_FLAG + 16 + 1024;         // + alignment slack
+  static constexpr int OFF_LG = OFF_FLAG + 16;              // logits of this CTA's keys (optional)
+  static constexpr int SMEM = OFF_LG + 1024;                // + alignment slack (+ logits bytes)
 };
+
+// Logits kept in shared memory for the in-kernel key mass: at most this many keys per CTA.
+constexpr int DM_LG_SMEM_KEYS = 1536;
 
 struct DmParams {
   int Hq, Hkv, G, R, T_cap, NT;
@@ -69,7 +73,11 @@ struct DmParams {
   int* counters;         // [R], zero on entry, left zero on exit
   float* out;            // [L, Hq, D]
   float* lse2;           // [R][8] (base-2 LSE per query head, for the key mass)
-  float* logits;         // [R][T_cap][8] or null
+  float* logits;         // [R][T_cap][8] in the workspace, or null
+  int lg_smem;           // 1: the logits of a CTA's keys stay in its shared memory instead
+  float* key_mass;       // [R][T_src] or null; in the cluster path accumulated in this kernel
+  const int32_t* key_pos;
+  int T_src;
   int* status;
   int cluster;           // > 0: the `cluster` CTAs of a row form a thread-block cluster and
                          // merge through distributed shared memory (no partials in HBM)
@@ -167,6 +175,7 @@ __global__ void __launch_bounds__(DM_THREADS, 2)
   float* sm_o = sm_l + DM_CWARPS * DM_QPAD;                           // [4][8][D]
   volatile int* flags = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);  // [0] abort, [1] last
   float* cst = reinterpret_cast<float*>(smem + C::OFF_CST);          // m[8], l[8], o[8][D]
+  float* sm_lg = reinterpret_cast<float*>(smem + C::OFF_LG);         // [keys of this CTA][8]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
@@ -189,13 +198,32 @@ __global__ void __launch_bounds__(DM_THREADS, 2)
 
   if (warp == DM_CWARPS) {
     // ------------------------------------------------------------ producer
+    if (p.key_mass && lane > 0) {
+      // Warm L2 with the key-mass entries (and source positions) this CTA adds to after the
+      // merge, so that the read-modify-writes at the end do not wait on DRAM.
+      const int r0 = (int)(x_begin / p.NT);
+      const int k_lo = (int)(x_begin - (long long)r0 * p.NT) * DM_TILE;
+      int k_hi = (int)(x_end - (long long)r0 * p.NT) * DM_TILE;
+      k_hi = k_hi < p.T_cap ? k_hi : p.T_cap;
+      if (x_end - x_begin > 0 && (x_end - 1) / p.NT == r0) {    // a range inside one row
+        for (int kk = k_lo + (lane - 1) * 32; kk < k_hi; kk += 31 * 32) {
+          if (p.key_pos)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(__cvta_generic_to_global(p.key_pos + (size_t)r0 * p.T_cap + kk)));
+          else
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(__cvta_generic_to_global(p.key_mass + (size_t)r0 * p.T_src + kk)));
+        }
+      }
+    }
     if (lane == 0) {
       ptx::prefetch_tmap(&tmK);
       ptx::prefetch_tmap(&tmV);
       int li = 0;
       for (long long x = x_begin; x < x_end; ++x) {
         const int r = (int)(x / p.NT), u = (int)(x % p.NT);
-        if (u * DM_TILE >= row_len(p, r)) continue;
+        // The first tile of the range is copied without waiting for the row length (it is
+        // inside the cache whatever the length); the consumers release it unread if it is
+        // past the end of the row.
+        if (x != x_begin && u * DM_TILE >= row_len(p, r)) continue;
         const int s = li % C::STAGES, use = li / C::STAGES;
         if (use > 0 && !ptx::mbar_wait(bar_empty + 8 * s, (use - 1) & 1, flags, p.status)) break;
         const uint32_t dst = sbase + s * C::STAGE_BYTES;
@@ -367,11 +395,17 @@ __global__ void __launch_bounds__(DM_THREADS, 2)
       }
       const int n = row_len(p, r);
       const int key_base = u * DM_TILE;
-      if (key_base >= n) continue;
+      if (key_base >= n && x != x_begin) continue;
       const int s = li % C::STAGES;
       // On a timeout every warp keeps walking the same tiles without computing, so the
       // row-segment barriers below are still reached by all four warps.
       if (!ptx::mbar_wait(bar_full + 8 * s, (li / C::STAGES) & 1, flags, p.status)) {
+        ++li;
+        continue;
+      }
+      if (key_base >= n) {                   // the speculative first tile of an empty range
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar_empty + 8 * s);
         ++li;
         continue;
       }
@@ -390,7 +424,11 @@ __global__ void __launch_bounds__(DM_THREADS, 2)
       const bool v0 = key0 < n, v1 = key1 < n;
       float x0 = v0 ? sc[0] * p.c2 : -INFINITY, x1 = v0 ? sc[1] * p.c2 : -INFINITY;
       float x2 = v1 ? sc[2] * p.c2 : -INFINITY, x3 = v1 ? sc[3] * p.c2 : -INFINITY;
-      if (p.logits) {
+      if (p.lg_smem) {
+        const int k0 = key0 - (int)(x_begin - (long long)r * p.NT) * DM_TILE;   // one row per CTA
+        if (v0) *reinterpret_cast<float2*>(sm_lg + k0 * DM_QPAD + 2 * t) = make_float2(x0, x1);
+        if (v1) *reinterpret_cast<float2*>(sm_lg + (k0 + 8) * DM_QPAD + 2 * t) = make_float2(x2, x3);
+      } else if (p.logits) {
         if (v0) *reinterpret_cast<float2*>(p.logits + ((size_t)r * p.T_cap + key0) * DM_QPAD + 2 * t) = make_float2(x0, x1);
         if (v1) *reinterpret_cast<float2*>(p.logits + ((size_t)r * p.T_cap + key1) * DM_QPAD + 2 * t) = make_float2(x2, x3);
       }
@@ -450,35 +488,124 @@ __global__ void __launch_bounds__(DM_THREADS, 2)
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();                          // every CTA of the row has its state in shared memory
-    if (cluster.block_rank() == 0 && warp < DM_CWARPS) {
-      const int k = (int)cluster.num_blocks();
-      const int r = c / k, l = r / p.Hkv, hk = r % p.Hkv;
-      const float* rs[8];
-      for (int rr = 0; rr < k; ++rr) rs[rr] = cluster.map_shared_rank(cst, rr);
-      for (int e = threadIdx.x; e < p.G * D; e += DM_CWARPS * 32) {
-        const int qh = e / D, d = e % D;
-        float mr[8], M = -INFINITY;
+    // Every CTA of the cluster forms the row's per-head max, weights and sum from the k
+    // states, then merges its own share of the G x D outputs (k independent remote loads
+    // per element, all in flight together).
+    const int k = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
+    const int r = c / k, l = r / p.Hkv, hk = r % p.Hkv;
+    __shared__ float wgt_sh[8][DM_QPAD];
+    __shared__ float lsum_sh[DM_QPAD], lse_sh[DM_QPAD];
+    if (warp < DM_CWARPS) {
+      if (threadIdx.x < DM_QPAD) {
+        const int qh = threadIdx.x;
+        float mr[8], lr[8], M = -INFINITY;
 #pragma unroll
         for (int rr = 0; rr < 8; ++rr) {
-          mr[rr] = rr < k ? rs[rr][qh] : -INFINITY;
+          mr[rr] = -INFINITY;
+          lr[rr] = 0.f;
+          if (rr < k) {
+            const float* rs = cluster.map_shared_rank(cst, rr);
+            mr[rr] = rs[qh];
+            lr[rr] = rs[DM_QPAD + qh];
+          }
           M = fmaxf(M, mr[rr]);
         }
-        float L = 0.f, O = 0.f;
-        if (M != -INFINITY) {
+        float L = 0.f;
 #pragma unroll
-          for (int rr = 0; rr < 8; ++rr) {
-            if (rr < k && mr[rr] != -INFINITY) {
-              const float wgt = fast_exp2(mr[rr] - M);
-              L = fmaf(rs[rr][DM_QPAD + qh], wgt, L);
-              O = fmaf(rs[rr][2 * DM_QPAD + qh * D + d], wgt, O);
-            }
-          }
+        for (int rr = 0; rr < 8; ++rr) {
+          const float wgt = (M == -INFINITY || mr[rr] == -INFINITY) ? 0.f : fast_exp2(mr[rr] - M);
+          wgt_sh[rr][qh] = wgt;
+          L = fmaf(lr[rr], wgt, L);
         }
-        p.out[((size_t)l * p.Hq + hk * p.G + qh) * D + d] = L > 0.f ? O / L : 0.f;
-        if (d == 0) p.lse2[r * DM_QPAD + qh] = L > 0.f ? M + __log2f(L) : -INFINITY;
+        lsum_sh[qh] = L;
+        lse_sh[qh] = L > 0.f ? M + __log2f(L) : -INFINITY;
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(DM_CWARPS * 32));
+      const float* ro[8];
+#pragma unroll
+      for (int rr = 0; rr < 8; ++rr) ro[rr] = cluster.map_shared_rank(cst, rr < k ? rr : 0) + 2 * DM_QPAD;
+      const int E = p.G * D, e_lo = rank * E / k, e_hi = (rank + 1) * E / k;
+      for (int e = e_lo + threadIdx.x; e < e_hi; e += DM_CWARPS * 32) {
+        const int qh = e / D;
+        float ov[8];
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) ov[rr] = rr < k ? ro[rr][e] : 0.f;
+        float O = 0.f;
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr)
+          if (rr < k) O = fmaf(ov[rr], wgt_sh[rr][qh], O);
+        const float L = lsum_sh[qh];
+        p.out[((size_t)l * p.Hq + hk * p.G) * D + e] = L > 0.f ? O / L : 0.f;
       }
     }
-    cluster.sync();                          // remote reads are done before any CTA exits
+    // Remote reads are finished (their values are used above); the barrier that keeps every
+    // CTA's shared memory alive until then is arrived at without release semantics, so the
+    // output stores need not drain first, and the key mass below overlaps the wait.
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    if (p.key_mass && warp < DM_CWARPS) {
+      // Key mass of this CTA's own keys: sum_g exp2(logit - lse2) for each key it scored.
+      const int n = row_len(p, r);
+      const int key_lo = (int)(x_begin - (long long)r * p.NT) * DM_TILE;
+      int key_hi = (int)(x_end - (long long)r * p.NT) * DM_TILE;
+      key_hi = key_hi < n ? key_hi : n;
+      float lse_r[DM_QPAD];
+#pragma unroll
+      for (int qh = 0; qh < DM_QPAD; ++qh) lse_r[qh] = qh < p.G ? lse_sh[qh] : INFINITY;
+      const int nk = key_hi - key_lo;
+      auto key_sum = [&](int j) -> float {          // sum_g exp2(logit - lse2) of key key_lo + j
+        const float* lg = p.lg_smem ? sm_lg + j * DM_QPAD
+                                    : p.logits + ((size_t)r * p.T_cap + key_lo + j) * DM_QPAD;
+        const float4 a = *reinterpret_cast<const float4*>(lg);
+        const float4 b = *reinterpret_cast<const float4*>(lg + 4);
+        return ((fast_exp2(a.x - lse_r[0]) + fast_exp2(a.y - lse_r[1])) +
+                (fast_exp2(a.z - lse_r[2]) + fast_exp2(a.w - lse_r[3]))) +
+               ((fast_exp2(b.x - lse_r[4]) + fast_exp2(b.y - lse_r[5])) +
+                (fast_exp2(b.z - lse_r[6]) + fast_exp2(b.w - lse_r[7])));
+      };
+      if (!p.key_pos && (p.T_src & 3) == 0 && (reinterpret_cast<uintptr_t>(p.key_mass) & 15) == 0) {
+        // Identity positions: this CTA alone owns its keys' entries, so a plain vector
+        // read-modify-write of four consecutive keys per thread replaces the atomics.
+        float* km = p.key_mass + (size_t)r * p.T_src + key_lo;
+        constexpr int STEP = 4 * DM_CWARPS * 32;
+        for (int j0 = 4 * threadIdx.x; j0 < nk; j0 += 2 * STEP) {
+          const int j1 = j0 + STEP;
+          float4 o0 = make_float4(0.f, 0.f, 0.f, 0.f), o1 = o0;
+          if (j0 + 3 < nk) o0 = *reinterpret_cast<const float4*>(km + j0);
+          if (j1 + 3 < nk) o1 = *reinterpret_cast<const float4*>(km + j1);
+          float m0[4], m1[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            m0[u] = j0 + u < nk ? key_sum(j0 + u) : 0.f;
+            m1[u] = j1 + u < nk ? key_sum(j1 + u) : 0.f;
+          }
+          if (j0 + 3 < nk) {
+            o0.x += m0[0]; o0.y += m0[1]; o0.z += m0[2]; o0.w += m0[3];
+            *reinterpret_cast<float4*>(km + j0) = o0;
+          } else {
+            for (int u = 0; u < 4; ++u)
+              if (j0 + u < nk) km[j0 + u] += m0[u];
+          }
+          if (j1 + 3 < nk) {
+            o1.x += m1[0]; o1.y += m1[1]; o1.z += m1[2]; o1.w += m1[3];
+            *reinterpret_cast<float4*>(km + j1) = o1;
+          } else {
+            for (int u = 0; u < 4; ++u)
+              if (j1 + u < nk) km[j1 + u] += m1[u];
+          }
+        }
+      } else {
+        for (int j = threadIdx.x; j < nk; j += DM_CWARPS * 32) {
+          const float pm = key_sum(j);
+          const int pos = p.key_pos ? p.key_pos[(size_t)r * p.T_cap + key_lo + j] : key_lo + j;
+          if (pos < 0 || pos >= p.T_src) {
+            raise_status(p.status, KVP_ERR_DEVICE_CHECK);
+            continue;
+          }
+          atomicAdd(p.key_mass + (size_t)r * p.T_src + pos, pm);
+        }
+      }
+    }
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
   } else {
     __syncthreads();
   }
@@ -569,18 +696,30 @@ cudaError_t run(const void* q, const void* kc, const void* vc, int dtype, int n_
   p.status = status;
   const int k = plan.n_ctas / plan.R;
   p.cluster = k <= 8 ? k : 0;
+  // cluster path: the key mass is added inside the decode kernel (logits in shared memory when
+  // a CTA's keys fit, else in the workspace); otherwise a second kernel adds it
+  p.lg_smem = key_mass && p.cluster && plan.lg_smem_keys > 0;
+  if (p.lg_smem) p.logits = nullptr;
+  p.key_mass = p.cluster ? key_mass : nullptr;
+  p.key_pos = key_pos;
+  p.T_src = T_src;
   cudaError_t e = cudaSuccess;
+  if (key_mass && !accumulate) {
+    e = cudaMemsetAsync(key_mass, 0, (size_t)plan.R * T_src * sizeof(float), st);
+    if (e != cudaSuccess) return e;
+  }
   if (!p.cluster) {
     e = cudaMemsetAsync(p.counters, 0, plan.counter_bytes, st);
     if (e != cudaSuccess) return e;
   }
+  const int smem_bytes = Dm<D>::SMEM + (p.lg_smem ? plan.lg_smem_keys * DM_QPAD * (int)sizeof(float) : 0);
   auto kern = decode_mma_kernel<T, D>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Dm<D>::SMEM);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)plan.n_ctas);
   cfg.blockDim = dim3(DM_THREADS);
-  cfg.dynamicSmemBytes = Dm<D>::SMEM;
+  cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -593,11 +732,7 @@ cudaError_t run(const void* q, const void* kc, const void* vc, int dtype, int n_
   e = cudaLaunchKernelEx(&cfg, kern, tk, tv, (const T*)q, p);
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
-  if (e != cudaSuccess || !key_mass) return e;
-  if (!accumulate) {
-    e = cudaMemsetAsync(key_mass, 0, (size_t)plan.R * T_src * sizeof(float), st);
-    if (e != cudaSuccess) return e;
-  }
+  if (e != cudaSuccess || !key_mass || p.cluster) return e;
   const long long total = (long long)plan.R * T_cap;
   long long blocks = (total + 255) / 256;
   if (blocks > 8192) blocks = 8192;
@@ -626,7 +761,12 @@ void decode_mma_plan(DecodePlan& p, int head_dim, int T_cap, int with_key_mass) 
   p.mma_partial_bytes = align256((size_t)p.n_ctas * p.maxseg * pstride * sizeof(float));
   p.counter_bytes = align256((size_t)p.R * sizeof(int));
   p.mma_lse_bytes = align256((size_t)p.R * DM_QPAD * sizeof(float));
-  p.mma_logit_bytes = with_key_mass ? align256((size_t)p.R * T_cap * DM_QPAD * sizeof(float)) : 0;
+  // logits of the in-kernel key mass: in shared memory when every CTA of a clustered row
+  // (k <= 8) scores at most DM_LG_SMEM_KEYS keys, else in the workspace
+  const long long keys_per_cta = (p.nt + k - 1) / k * DM_TILE;
+  p.lg_smem_keys = (with_key_mass && k <= 8 && keys_per_cta <= DM_LG_SMEM_KEYS) ? (int)keys_per_cta : 0;
+  p.mma_logit_bytes = with_key_mass && !p.lg_smem_keys
+                          ? align256((size_t)p.R * T_cap * DM_QPAD * sizeof(float)) : 0;
   p.mma_total_bytes = p.mma_partial_bytes + p.counter_bytes + p.mma_lse_bytes + p.mma_logit_bytes;
 }
 

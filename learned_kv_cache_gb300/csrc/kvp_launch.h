@@ -56,6 +56,7 @@ struct DecodePlan {
   size_t partial_bytes, lse_bytes, logit_bytes, simt_total_bytes;
   // bf16/f16 cache path (persistent stream-K CTAs over 64-key tiles)
   int nt, n_ctas, maxseg;
+  int lg_smem_keys;     // > 0: the key-mass logits of a CTA stay in shared memory (keys per CTA)
   size_t mma_partial_bytes, counter_bytes, mma_lse_bytes, mma_logit_bytes, mma_total_bytes;
   size_t total_bytes;   // workspace that covers either path
 };

@@ -47,6 +47,42 @@ def test_decode_ragged_lengths(kvp, dtype, D, G):
     _mass_close(mass.cpu().numpy(), 2 * mref)
 
 
+@pytest.mark.parametrize("L,Hkv,T_cap,use_pos", [
+    (6, 2, 3000, False),     # rows split over a cluster of CTAs, logits in shared memory
+    (20, 2, 12000, True),    # cluster, more keys per CTA than shared memory holds: workspace logits
+    (1, 2, 20000, True),     # more than 8 CTAs per row: partials merged by the last CTA, second pass
+])
+def test_decode_key_mass_paths(kvp, L, Hkv, T_cap, use_pos):
+    """The key mass through each way the decode kernel can form it, with ragged lengths,
+    optional source positions and accumulation."""
+    G, D = 4, 128
+    R = L * Hkv
+    gen = torch.Generator().manual_seed(T_cap + R)
+    q = torch.randn(L, G * Hkv, D, generator=gen).to(torch.bfloat16)
+    kc = (torch.randn(R, T_cap, D, generator=gen) * 1.5).to(torch.bfloat16)
+    vc = torch.randn(R, T_cap, D, generator=gen).to(torch.bfloat16)
+    lens = torch.randint(T_cap // 2, T_cap + 1, (R,), generator=gen).to(torch.int32)
+    lens[0] = T_cap
+    T_src = T_cap * 2 if use_pos else T_cap
+    pos = None
+    if use_pos:
+        pos = torch.stack([torch.randperm(T_src, generator=gen)[:T_cap].sort().values
+                           for _ in range(R)]).to(torch.int32)
+    mass = torch.full((R, T_src), 3.0, device="cuda")
+    out = kvp.kvp_decode_attn(q.cuda(), kc.cuda(), vc.cuda(), lens.cuda(), key_mass=mass,
+                              key_pos=None if pos is None else pos.cuda())
+    torch.cuda.synchronize()
+    kvp.kvp_check_device_status()
+    ref, mref = oracle.decode_attn(q, kc, vc, lens.numpy(), D ** -0.5,
+                                   key_pos=None if pos is None else pos.numpy(), T_src=T_src)
+    assert np.abs(out.cpu().double().numpy() - ref).max() <= DECODE_ATOL
+    _mass_close(mass.cpu().numpy(), mref)
+    kvp.kvp_decode_attn(q.cuda(), kc.cuda(), vc.cuda(), lens.cuda(), key_mass=mass,
+                        key_pos=None if pos is None else pos.cuda(), accumulate=True)
+    torch.cuda.synchronize()
+    _mass_close(mass.cpu().numpy(), 2 * mref)
+
+
 def test_decode_single_key_and_identical_keys(kvp):
     D = 128
     v = torch.randn(2, 64, D).to(torch.bfloat16)

@@ -25,6 +25,7 @@ def kvp():
 @pytest.mark.parametrize("dtype,D,cap,n_sink,n_recent,steps", [
     (torch.float16, 128, 48, 4, 8, 160),
     (torch.bfloat16, 64, 32, 2, 3, 120),
+    (torch.bfloat16, 128, 37, 1, 5, 100),
 ])
 def test_ring_stream_matches_oracle(kvp, dtype, D, cap, n_sink, n_recent, steps):
     L, Hkv, G = 2, 2, 3
