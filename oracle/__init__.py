@@ -16,6 +16,9 @@ Functions and the passages they follow:
 * :func:`decode_attn` -- How much KV cache can you prune, "Bounded windows".
 * :func:`ring_victim`, :func:`ring_insert` -- How much KV cache can you prune,
   "What we did" and "Conclusion" (static cache overwritten in place).
+* :func:`fenwick_cutoffs`, :func:`sparse_mask`, :func:`sparse_row_lse` -- KVpop, "Efficient
+  Online Pruning", "Fenwick-tree cut-off computation (Algorithm 2)" and "Delayed Memory
+  Scoring" (the sparse log-normalisers).
 * :func:`soft_topk`, :func:`head_budgets` -- LKV, "The Differentiable Soft-TopK
   Operator" and "LKV-H".
 
@@ -26,10 +29,12 @@ pages' worked examples).
 from .attention_mass import future_attn_mass, future_attn_mass_per_head, kvpop_target, row_lse
 from .budgets import head_budgets, soft_topk
 from .decode import decode_attn
+from .fenwick import fenwick_cutoffs, sparse_mask, sparse_row_lse
 from .ring import ring_insert, ring_victim
 from .selection import compact_kv, effective_budget, select_row, select_topk
 
 __all__ = [
     "row_lse", "future_attn_mass", "future_attn_mass_per_head", "kvpop_target", "select_topk", "select_row", "effective_budget",
     "compact_kv", "decode_attn", "soft_topk", "head_budgets", "ring_insert", "ring_victim",
+    "fenwick_cutoffs", "sparse_mask", "sparse_row_lse",
 ]
