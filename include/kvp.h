@@ -10,6 +10,11 @@
  *   kvp_compact_kv         gather of the kept K/V rows into a dense pruned cache
  *   kvp_decode_attn        one-token decode attention over the (pruned) cache
  *
+ * and the steps either side of them: kvp_future_attn_target (KVpop's supervision
+ * target), kvp_ring_insert (in-place eviction of a static decode cache),
+ * kvp_topk_cutoffs and kvp_sparse_lse_pass (KVpop's running top-k sparse
+ * attention and its log-normalisers).
+ *
  * Conventions shared by every entry point
  * ---------------------------------------
  * - Every pointer argument is a DEVICE pointer unless stated otherwise; the
@@ -133,6 +138,47 @@ int kvp_future_attn_target(const void* q, const void* k, const float* lse, int d
                            int h_q, int h_kv, int seq_len, int head_dim, float sm_scale,
                            int window, float eps, int aggregate, float* target, float* F_heads,
                            float* F, void* workspace, size_t workspace_bytes, kvp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * A1'. Running top-k cutoffs (KVpop's online pruning during prefill/training).
+ *
+ * KVpop, "Efficient Online Pruning" and "Fenwick-tree cut-off computation
+ * (Algorithm 2)": every token of a KV head has a static rank (0 = most
+ * important; a permutation of 0..seq_len-1 per head).  At query q the token
+ * t = q - window leaves the protected window and becomes eligible unless
+ * t < n_sink.  Once k tokens are eligible, tau[h, q] is the k-th smallest rank
+ * among the eligible tokens (the rank threshold of the top-k eligible set);
+ * before that tau[h, q] = -1.  The page keeps the eligible ranks in a Fenwick
+ * tree; this library computes the same thresholds with per-chunk bitmaps.
+ *
+ * ranks [n_heads, seq_len] int32 (input), tau [n_heads, seq_len] int32 (output).
+ * 1 <= seq_len <= 1048576, k >= 1, n_sink >= 0, window >= 0.  Ranks that are
+ * out of range or repeated are reported through the device status
+ * (KVP_ERR_DEVICE_CHECK) and leave tau unspecified.
+ * ------------------------------------------------------------------------- */
+int kvp_topk_cutoffs(const int32_t* ranks, int n_heads, int seq_len, int n_sink, int window,
+                     int k, int32_t* tau, kvp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * A1''. Sparse row log-sum-exp (the student's log-normalisers).
+ *
+ * KVpop, "Efficient Online Pruning" (query q attends to the sink tokens, the
+ * protected window and the eligible tokens of rank <= tau_q) and "Delayed
+ * Memory Scoring" (the future-attention target reuses these sparse
+ * log-normalisers; pass the result as `lse` to kvp_future_attn_mass or
+ * kvp_future_attn_target):
+ *
+ *   keep(i, j) = j <= i and (j < n_sink or j > i - window or tau[i] < 0 or rank[j] <= tau[i])
+ *   lse[b, h, i] = ln sum_{j : keep(i, j)} exp(sm_scale * q[b, h, i] . k[b, h/G, j])
+ *
+ * tau[i] < 0 (fewer than k eligible tokens) keeps every eligible token.
+ * q, k, lse as in kvp_lse_pass; ranks and tau [n_batch, h_kv, seq_len] int32
+ * (kvp_topk_cutoffs' input and output; any int32 values are accepted, the
+ * mask is applied as written).
+ * ------------------------------------------------------------------------- */
+int kvp_sparse_lse_pass(const void* q, const void* k, const int32_t* ranks, const int32_t* tau,
+                        int dtype, int n_batch, int h_q, int h_kv, int seq_len, int head_dim,
+                        float sm_scale, int n_sink, int window, float* lse, kvp_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * A0. Head-wise budgets from the closed-form Soft-TopK.

@@ -113,3 +113,10 @@ def make_scores(R: int, T: int, seed: int, device="cpu", quantize: int | None = 
                             device=device, dtype=torch.float32)
         s.scatter_(1, idx, vals.expand(R, 12).contiguous())
     return s
+
+
+def make_static_ranks(H: int, S: int, seed: int, device="cpu") -> torch.Tensor:
+    """Seeded static token ranks: one random permutation of 0..S-1 per KV head (int32 [H, S]),
+    standing in for the ranks a trained scorer's static priorities would give."""
+    gen = _generator(seed, device)
+    return torch.stack([torch.randperm(S, generator=gen, device=device) for _ in range(H)]).to(torch.int32)

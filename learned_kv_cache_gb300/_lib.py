@@ -31,6 +31,8 @@ SIGNATURES = {
     "kvp_future_attn_target_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "kvp_future_attn_target": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _F, _I, _P, _P, _P, _P,
                                     _SZ, _P]),
+    "kvp_topk_cutoffs": (_I, [_P, _I, _I, _I, _I, _I, _P, _P]),
+    "kvp_sparse_lse_pass": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P]),
     "kvp_soft_topk_budgets": (_I, [_P, _I, _D, _I, _P, _P, _P]),
     "kvp_select_topk": (_I, [_P, _I, _I, _I64, _P, _I, _I, _P, _I, _P, _P]),
     "kvp_compact_kv": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P]),
@@ -133,6 +135,47 @@ def kvp_lse_pass(q, k, sm_scale=None, lse=None, stream=None):
     rc = load().kvp_lse_pass(_ptr(q4), _ptr(k4), _dtype(q4), B, Hq, Hkv, S, D, float(sm_scale),
                              _ptr(lse), _stream(stream))
     _check("kvp_lse_pass", rc)
+    return lse[0] if squeeze and lse.dim() == 3 else lse
+
+
+def kvp_topk_cutoffs(ranks, n_sink, window, k, tau=None, stream=None):
+    """Running top-k cutoffs: ranks int32 [..., S] (one row per KV head) -> tau int32 [..., S]."""
+    _need(ranks, "ranks", torch.int32)
+    S = ranks.shape[-1]
+    H = ranks.numel() // max(S, 1)
+    if tau is None:
+        tau = torch.empty_like(ranks)
+    _need(tau, "tau", torch.int32, tuple(ranks.shape))
+    rc = load().kvp_topk_cutoffs(_ptr(ranks), H, S, int(n_sink), int(window), int(k), _ptr(tau),
+                                 _stream(stream))
+    _check("kvp_topk_cutoffs", rc)
+    return tau
+
+
+def kvp_sparse_lse_pass(q, k, ranks, tau, n_sink, window, sm_scale=None, lse=None, stream=None):
+    """Sparse row LSE under the running top-k mask: q [B,H_q,S,D], k [B,H_kv,S,D], ranks and
+    tau int32 [B,H_kv,S] -> lse fp32 [B,H_q,S]."""
+    squeeze = q.dim() == 3
+    q4, k4 = _bhsd(q, k)
+    B, Hq, S, D = q4.shape
+    Hkv = k4.shape[1]
+    _need(q4, "q")
+    _need(k4, "k", dtype=q4.dtype, shape=(B, Hkv, S, D))
+    _need(ranks, "ranks", torch.int32)
+    _need(tau, "tau", torch.int32)
+    if ranks.numel() != B * Hkv * S or tau.numel() != B * Hkv * S:
+        raise ValueError("ranks / tau must hold n_batch * h_kv * seq_len entries")
+    if sm_scale is None:
+        sm_scale = D ** -0.5
+    if lse is None:
+        lse = torch.empty(B, Hq, S, device=q.device, dtype=torch.float32)
+    _need(lse, "lse", torch.float32)
+    if lse.numel() != B * Hq * S:
+        raise ValueError("lse has the wrong size")
+    rc = load().kvp_sparse_lse_pass(_ptr(q4), _ptr(k4), _ptr(ranks), _ptr(tau), _dtype(q4), B, Hq, Hkv,
+                                    S, D, float(sm_scale), int(n_sink), int(window), _ptr(lse),
+                                    _stream(stream))
+    _check("kvp_sparse_lse_pass", rc)
     return lse[0] if squeeze and lse.dim() == 3 else lse
 
 

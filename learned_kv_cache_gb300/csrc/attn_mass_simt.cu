@@ -13,6 +13,8 @@
 //    columns = queries i >= j + w of every query head of the group; each
 //    thread accumulates exp2(s*log2e*scale - lse_i*log2e) of its patch rows,
 //    reduced across the 16 threads of a row at the end.
+#include <climits>
+
 #include "kvp_common.cuh"
 #include "kvp_launch.h"
 
@@ -74,10 +76,15 @@ __device__ __forceinline__ float row_sum16(float v) {
   return v;
 }
 
+// ranks != null: the sparse row LSE (running top-k mask: key j is kept for query i if
+// j < n_sink, j > i - window, tau_i < 0 or rank_j <= tau_i).
 template <typename T, int D>
 __global__ void __launch_bounds__(256) lse_simt_kernel(const T* __restrict__ q,
                                                        const T* __restrict__ k, int Hq, int Hkv,
-                                                       int S, float c2, float* __restrict__ lse) {
+                                                       int S, float c2, float* __restrict__ lse,
+                                                       const int32_t* __restrict__ ranks,
+                                                       const int32_t* __restrict__ tau, int n_sink,
+                                                       int window) {
   extern __shared__ float sm[];
   float* As = sm;
   float* Bs = sm + D * LD;
@@ -87,6 +94,14 @@ __global__ void __launch_bounds__(256) lse_simt_kernel(const T* __restrict__ q,
   const T* kh = k + (size_t)(b * Hkv + hq / G) * S * D;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   load_tile_t<T, D>(As, qh, i0, S);
+  const int32_t* rk = ranks ? ranks + (size_t)(b * Hkv + hq / G) * S : nullptr;
+  int tau_r[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int i = i0 + ty * 4 + a;
+    const int tq = (rk && i < S) ? tau[(size_t)(b * Hkv + hq / G) * S + i] : -1;
+    tau_r[a] = tq < 0 ? INT_MAX : tq;
+  }
   float m[4], l[4];
 #pragma unroll
   for (int a = 0; a < 4; ++a) { m[a] = -INFINITY; l[a] = 0.f; }
@@ -104,7 +119,9 @@ __global__ void __launch_bounds__(256) lse_simt_kernel(const T* __restrict__ q,
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int j = j0 + tx * 4 + c;
-        s2[c] = (j <= i && j < S) ? acc[a][c] * c2 : -INFINITY;
+        bool keep = j <= i && j < S;
+        if (keep && rk && j >= n_sink && j <= i - window) keep = rk[j] <= tau_r[a];
+        s2[c] = keep ? acc[a][c] * c2 : -INFINITY;
         tmax = fmaxf(tmax, s2[c]);
       }
       tmax = row_max16(tmax);
@@ -222,14 +239,16 @@ __global__ void target_epilogue_kernel(const float* __restrict__ Fh, int Hq, int
 
 template <typename T, int D>
 cudaError_t lse_simt(const void* q, const void* k, AttnShape s, float scale, float* lse,
-                     cudaStream_t st) {
+                     cudaStream_t st, const SparseMask* mask) {
   const size_t smem = 2 * D * LD * sizeof(float);
   auto kern = lse_simt_kernel<T, D>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   dim3 grid((s.seq_len + TM - 1) / TM, s.h_q, s.n_batch);
   count_launches(1);
   kern<<<grid, 256, smem, st>>>((const T*)q, (const T*)k, s.h_q, s.h_kv, s.seq_len,
-                                scale * KVP_LOG2E, lse);
+                                scale * KVP_LOG2E, lse, mask ? mask->ranks : nullptr,
+                                mask ? mask->tau : nullptr, mask ? mask->n_sink : 0,
+                                mask ? mask->window : 0);
   return cudaGetLastError();
 }
 
@@ -249,15 +268,15 @@ cudaError_t fam_simt(const void* q, const void* k, const float* lse, AttnShape s
 }  // namespace
 
 cudaError_t launch_lse_simt(const void* q, const void* k, int dtype, AttnShape s, float scale,
-                            float* lse, cudaStream_t st) {
+                            float* lse, cudaStream_t st, const SparseMask* mask) {
   const bool d128 = s.head_dim == 128;
   switch (dtype) {
-    case KVP_F32: return d128 ? lse_simt<float, 128>(q, k, s, scale, lse, st)
-                              : lse_simt<float, 64>(q, k, s, scale, lse, st);
-    case KVP_BF16: return d128 ? lse_simt<__nv_bfloat16, 128>(q, k, s, scale, lse, st)
-                               : lse_simt<__nv_bfloat16, 64>(q, k, s, scale, lse, st);
-    default: return d128 ? lse_simt<__half, 128>(q, k, s, scale, lse, st)
-                         : lse_simt<__half, 64>(q, k, s, scale, lse, st);
+    case KVP_F32: return d128 ? lse_simt<float, 128>(q, k, s, scale, lse, st, mask)
+                              : lse_simt<float, 64>(q, k, s, scale, lse, st, mask);
+    case KVP_BF16: return d128 ? lse_simt<__nv_bfloat16, 128>(q, k, s, scale, lse, st, mask)
+                               : lse_simt<__nv_bfloat16, 64>(q, k, s, scale, lse, st, mask);
+    default: return d128 ? lse_simt<__half, 128>(q, k, s, scale, lse, st, mask)
+                         : lse_simt<__half, 64>(q, k, s, scale, lse, st, mask);
   }
 }
 

@@ -9,6 +9,11 @@
 //  * row LSE (KVpop, "Delayed Memory Scoring", LSE worked example): A = a
 //    query tile, B = the key tiles 0..qt (causal); each TMEM lane is one query
 //    row; online max / sum in base 2; the diagonal tile is masked j <= i.
+//  * sparse row LSE (KVpop, "Efficient Online Pruning" and "Delayed Memory
+//    Scoring": the student's sparse log-normalisers): the row-LSE pass with the
+//    running top-k mask applied per element before the exp -- sinks, the
+//    protected window and the eligible keys whose static rank is within the
+//    query's cutoff.
 //  * future-attention mass (KVpop, Figure 2, transposed attention): roles
 //    swapped, A = a key tile, B = the query tiles i >= j + w of every query
 //    head of the GQA group; each TMEM lane is one key row and simply
@@ -32,6 +37,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <climits>
 #include <mutex>
 
 #include "kvp_common.cuh"
@@ -95,6 +101,12 @@ struct TcParams {
   int NQT;               // LSE pass: query tiles per head
   int NT0, TPC, CMAX, NKT, Nf;   // mass pass schedule
   int per_head;          // mass pass: keep each query head's sum (partials [.., G, 2 halves, 128])
+  // sparse LSE pass (MODE 2): static ranks and running cutoffs [B*Hkv*S] of the running top-k
+  // mask; key j is kept for query i if j < n_sink, j > i - window, tau_i < 0 or rank_j <= tau_i
+  const int32_t* ranks;
+  const int32_t* tau;
+  int n_sink;
+  int ranks_vec;         // ranks rows are 16-byte aligned (S % 4 == 0): int4 loads
   int* status;
 };
 
@@ -109,7 +121,7 @@ struct Item {
 template <int MODE>
 __device__ __forceinline__ Item decode_item(int I, const TcParams& p) {
   Item it;
-  if (MODE == 0) {
+  if (MODE != 1) {
     it.group = I % p.n_groups;
     it.tile = p.NQT - 1 - I / p.n_groups;
     it.chunk = 0;
@@ -243,7 +255,7 @@ __global__ void __launch_bounds__(THREADS, 2)
 
   // Coordinates of the fixed A tile and of streamed tile t.
   int a_row, a_z, kv_z = 0, b_of_group = 0, hkv = 0;
-  if (MODE == 0) {
+  if (MODE != 1) {
     a_row = it.tile * BM;
     a_z = it.group;
     b_of_group = it.group / p.Hq;
@@ -256,7 +268,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   }
   const int j0 = it.tile * BM;     // mass pass: first key of the tile
   auto b_coords = [&](int t, int& row, int& z) {
-    if (MODE == 0) {
+    if (MODE != 1) {
       row = t * BN;
       z = kv_z;
     } else {
@@ -267,8 +279,8 @@ __global__ void __launch_bounds__(THREADS, 2)
   };
 
   if (warp == PRODUCER_WARP) {
-    const CUtensorMap* tmA = MODE == 0 ? &tmQ : &tmK;
-    const CUtensorMap* tmB = MODE == 0 ? &tmK : &tmQ;
+    const CUtensorMap* tmA = MODE != 1 ? &tmQ : &tmK;
+    const CUtensorMap* tmB = MODE != 1 ? &tmK : &tmQ;
     if (lane == 0) {
       ptx::mbar_arrive_expect_tx(bar_a, TILE_BYTES);
       ptx::tma_load_3d(sA, tmA, bar_a, 0, a_row, a_z);
@@ -360,6 +372,14 @@ __global__ void __launch_bounds__(THREADS, 2)
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     uint64_t acc01 = 0, acc23 = 0;                           // mass pass: packed fp32 pairs
     float m = -INFINITY, l = 0.f;                            // LSE pass running state
+    const int row_i = it.tile * BM + r;                       // LSE passes: query of this row
+    const int32_t* ranks_row = nullptr;                      // sparse LSE: ranks of the KV head
+    int tau_eff = INT_MAX;                                   // sparse LSE: cutoff (none: INT_MAX)
+    if (MODE == 2) {
+      ranks_row = p.ranks + (size_t)kv_z * p.S;
+      const int tq = row_i < p.S ? __ldg(p.tau + (size_t)kv_z * p.S + row_i) : -1;
+      tau_eff = tq < 0 ? INT_MAX : tq;
+    }
     bool ok = true;
     const uint64_t c2x2 = pack2(p.c2, p.c2);
     for (int t = 0; t < it.n_tiles; ++t) {
@@ -379,12 +399,40 @@ __global__ void __launch_bounds__(THREADS, 2)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar_acce + 8 * a);
 
-      if (MODE == 0) {
+      if (MODE != 1) {
         const bool diag = (t == it.tile);
         if (diag) {
 #pragma unroll
           for (int c = 0; c < 64; ++c)
             if (half * 64 + c > r) v[c] = __float_as_uint(-INFINITY);
+        }
+        if (MODE == 2) {
+          // Columns cs <= c <= cw are eligible (neither sink nor in the protected window) and
+          // are dropped when their rank is past the row's cutoff.
+          const int jb = t * BN + half * 64;
+          const int cw = row_i - p.window - jb, cs = p.n_sink - jb;
+          const int lo = cs > 0 ? cs : 0, hi = cw < 63 ? cw : 63;
+          if (__any_sync(0xffffffffu, tau_eff != INT_MAX && lo <= hi)) {
+            const int32_t* rk = ranks_row + jb;
+            if (p.ranks_vec && jb + 64 <= p.S) {
+#pragma unroll
+              for (int g4 = 0; g4 < 16; ++g4) {
+                const int4 r4 = __ldg(reinterpret_cast<const int4*>(rk) + g4);
+                const int rr[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const int c = 4 * g4 + u;
+                  if (c >= lo && c <= hi && rr[u] > tau_eff) v[c] = __float_as_uint(-INFINITY);
+                }
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < 64; ++c) {
+                if (c >= lo && c <= hi && jb + c < p.S && __ldg(rk + c) > tau_eff)
+                  v[c] = __float_as_uint(-INFINITY);
+              }
+            }
+          }
         }
         float tm = -INFINITY;
 #pragma unroll
@@ -442,7 +490,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
     // Combine the two column halves of every row and write the result.
     asm volatile("bar.sync 1, %0;" ::"r"(EPI_WARPS * 32));
-    if (MODE == 0) {
+    if (MODE != 1) {
       if (half == 1) {
         red[r] = m;
         red[BM + r] = l;
@@ -598,7 +646,7 @@ size_t fam_tc_workspace_size(AttnShape s, int window, int per_head) {
 }
 
 cudaError_t launch_lse_tc(const void* q, const void* k, int dtype, AttnShape s, float scale,
-                          float* lse, int* status, cudaStream_t st) {
+                          float* lse, int* status, cudaStream_t st, const SparseMask* mask) {
   CUtensorMap tq, tk;
   if (!make_tmap(&tq, q, dtype, s.n_batch * s.h_q, s.seq_len) ||
       !make_tmap(&tk, k, dtype, s.n_batch * s.h_kv, s.seq_len))
@@ -613,6 +661,14 @@ cudaError_t launch_lse_tc(const void* q, const void* k, int dtype, AttnShape s, 
   p.n_groups = s.n_batch * s.h_q;
   p.NQT = (s.seq_len + BM - 1) / BM;
   p.status = status;
+  if (mask) {
+    p.ranks = mask->ranks;
+    p.tau = mask->tau;
+    p.n_sink = mask->n_sink;
+    p.window = mask->window;
+    p.ranks_vec = s.seq_len % 4 == 0 && ((uintptr_t)mask->ranks & 15) == 0;
+    return launch_tc<2>(tq, tk, p, p.n_groups * p.NQT, dtype == KVP_BF16, st);
+  }
   return launch_tc<0>(tq, tk, p, p.n_groups * p.NQT, dtype == KVP_BF16, st);
 }
 

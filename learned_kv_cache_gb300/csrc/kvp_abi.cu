@@ -148,6 +148,43 @@ int kvp_lse_pass(const void* q, const void* k, int dtype, int n_batch, int h_q, 
   return KVP_OK;
 }
 
+int kvp_topk_cutoffs(const int32_t* ranks, int n_heads, int seq_len, int n_sink, int window, int k,
+                     int32_t* tau, kvp_stream_t stream) {
+  g_last_error.clear();
+  if (!ranks || !tau) return fail(KVP_ERR_INVALID_ARG, "null ranks/tau");
+  if (n_heads < 1 || n_heads > 65535) return fail(KVP_ERR_INVALID_ARG, "n_heads=%d", n_heads);
+  if (seq_len < 1 || seq_len > (1 << 20)) return fail(KVP_ERR_INVALID_ARG, "seq_len=%d", seq_len);
+  if (k < 1) return fail(KVP_ERR_INVALID_ARG, "k=%d must be >= 1", k);
+  if (n_sink < 0 || window < 0) return fail(KVP_ERR_INVALID_ARG, "n_sink=%d window=%d", n_sink, window);
+  int* st = nullptr;
+  KVP_TRY(status_ptr(&st));
+  cudaError_t e = kvp::launch_topk_cutoffs(ranks, n_heads, seq_len, n_sink, window, k, tau, st,
+                                           (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kvp_topk_cutoffs launch");
+  return KVP_OK;
+}
+
+int kvp_sparse_lse_pass(const void* q, const void* k, const int32_t* ranks, const int32_t* tau,
+                        int dtype, int n_batch, int h_q, int h_kv, int seq_len, int head_dim,
+                        float sm_scale, int n_sink, int window, float* lse, kvp_stream_t stream) {
+  g_last_error.clear();
+  KVP_TRY(check_dtype(dtype));
+  KVP_TRY(check_attn_shape(n_batch, h_q, h_kv, seq_len, head_dim));
+  if (!q || !k || !lse || !ranks || !tau) return fail(KVP_ERR_INVALID_ARG, "null q/k/ranks/tau/lse");
+  if (!aligned16(q) || !aligned16(k)) return fail(KVP_ERR_INVALID_ARG, "q/k not 16-byte aligned");
+  if (!std::isfinite(sm_scale)) return fail(KVP_ERR_INVALID_ARG, "sm_scale not finite");
+  if (n_sink < 0 || window < 0) return fail(KVP_ERR_INVALID_ARG, "n_sink=%d window=%d", n_sink, window);
+  int* st = nullptr;
+  KVP_TRY(status_ptr(&st));
+  kvp::AttnShape s{n_batch, h_q, h_kv, seq_len, head_dim};
+  const kvp::SparseMask mask{ranks, tau, n_sink, window};
+  cudaError_t e = kvp::tc_supported(dtype, s)
+                      ? kvp::launch_lse_tc(q, k, dtype, s, sm_scale, lse, st, (cudaStream_t)stream, &mask)
+                      : kvp::launch_lse_simt(q, k, dtype, s, sm_scale, lse, (cudaStream_t)stream, &mask);
+  if (e != cudaSuccess) return cuda_fail(e, "kvp_sparse_lse_pass launch");
+  return KVP_OK;
+}
+
 size_t kvp_future_attn_mass_workspace_size(int dtype, int n_batch, int h_q, int h_kv, int seq_len,
                                            int head_dim, int window) {
   if (check_dtype(dtype) != KVP_OK || check_attn_shape(n_batch, h_q, h_kv, seq_len, head_dim) != KVP_OK ||

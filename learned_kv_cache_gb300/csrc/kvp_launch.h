@@ -15,9 +15,17 @@ struct AttnShape {
   int n_batch, h_q, h_kv, seq_len, head_dim;
 };
 
-// fp32-FFMA tiled passes (any dtype; the only path for float32 inputs).
+// Running top-k mask of the sparse row LSE: static ranks and cutoffs [n_batch*h_kv, S].
+struct SparseMask {
+  const int32_t* ranks;
+  const int32_t* tau;
+  int n_sink, window;
+};
+
+// fp32-FFMA tiled passes (any dtype; the only path for float32 inputs).  mask != null: the
+// sparse row LSE.
 cudaError_t launch_lse_simt(const void* q, const void* k, int dtype, AttnShape s, float scale,
-                            float* lse, cudaStream_t st);
+                            float* lse, cudaStream_t st, const SparseMask* mask = nullptr);
 cudaError_t launch_fam_simt(const void* q, const void* k, const float* lse, int dtype, AttnShape s,
                             float scale, int window, float* F, cudaStream_t st, int per_head = 0);
 // KVpop target from per-query-head mass: count normalisation, log(eps + m), group max / mean.
@@ -29,7 +37,7 @@ cudaError_t launch_target_epilogue(const float* F_heads, int n_batch, int h_q, i
 bool tc_supported(int dtype, AttnShape s);
 size_t fam_tc_workspace_size(AttnShape s, int window, int per_head = 0);
 cudaError_t launch_lse_tc(const void* q, const void* k, int dtype, AttnShape s, float scale,
-                          float* lse, int* status, cudaStream_t st);
+                          float* lse, int* status, cudaStream_t st, const SparseMask* mask = nullptr);
 // per_head = 1: F receives each query head's mass, [n_batch, h_q, seq_len].
 cudaError_t launch_fam_tc(const void* q, const void* k, const float* lse, int dtype, AttnShape s,
                           float scale, int window, float* F, void* ws, size_t ws_bytes,
@@ -43,6 +51,10 @@ cudaError_t launch_select(const float* scores, int R, int T, int64_t row_stride,
 cudaError_t launch_compact(const void* k, const void* v, int row_bytes, int R, int T,
                            const int32_t* idx, const int32_t* count, int b_max, void* k_out,
                            void* v_out, int* status, cudaStream_t st);
+
+// Running top-k cutoffs tau [n_heads, S] from static ranks (a permutation of 0..S-1 per head).
+cudaError_t launch_topk_cutoffs(const int32_t* ranks, int n_heads, int S, int n_sink, int window,
+                                int k, int32_t* tau, int* status, cudaStream_t st);
 
 cudaError_t launch_ring_insert(void* kc, void* vc, int32_t* slot_pos, float* slot_score, int32_t* fill,
                                int R, int cap, int row_bytes, const void* new_k, const void* new_v,

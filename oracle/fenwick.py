@@ -103,21 +103,30 @@ def sparse_mask(ranks, tau, n_sink: int, window: int) -> np.ndarray:
     return causal & (protected | top)
 
 
-def sparse_row_lse(q, k, ranks, tau, scale: float, n_sink: int, window: int) -> np.ndarray:
+def sparse_row_lse(q, k, ranks, tau, scale: float, n_sink: int, window: int, rows=None) -> np.ndarray:
     """lse[h_q, i] = ln sum_{j kept for (h_q // G, i)} exp(scale * q[h_q, i] . k[h_q // G, j]).
 
-    q: [H_q, S, D]; k: [H_kv, S, D]; ranks, tau: [H_kv, S]."""
+    q: [H_q, S, D]; k: [H_kv, S, D]; ranks, tau: [H_kv, S].  ``rows`` optionally lists the query
+    positions to evaluate (the result then has shape [H_q, len(rows)])."""
     q = _as_f64(q)
     k = _as_f64(k)
+    ranks = np.asarray(ranks, dtype=np.int64)
+    tau = np.asarray(tau, dtype=np.int64)
     Hq, S, _ = q.shape
     Hkv = k.shape[0]
     G = Hq // Hkv
-    out = np.empty((Hq, S))
+    rows = np.arange(S) if rows is None else np.asarray(rows, dtype=np.int64)
+    out = np.empty((Hq, rows.size))
+    jj = np.arange(S)[None, :]
+    blk = max(1, (1 << 22) // max(S, 1))
     for h in range(Hkv):
-        keep = sparse_mask(ranks[h], tau[h], n_sink, window)
-        for g in range(G):
-            s = (q[h * G + g] @ k[h].T) * scale
-            s = np.where(keep, s, -np.inf)
-            m = s.max(axis=1, keepdims=True)
-            out[h * G + g] = m[:, 0] + np.log(np.exp(s - m).sum(axis=1))
+        for b0 in range(0, rows.size, blk):
+            ii = rows[b0:b0 + blk][:, None]
+            t = tau[h][ii]
+            keep = (jj <= ii) & ((jj < n_sink) | (jj > ii - window) | (t < 0) | (ranks[h][None, :] <= t))
+            for g in range(G):
+                s = (q[h * G + g, ii[:, 0]] @ k[h].T) * scale
+                s = np.where(keep, s, -np.inf)
+                m = s.max(axis=1, keepdims=True)
+                out[h * G + g, b0:b0 + blk] = m[:, 0] + np.log(np.exp(s - m).sum(axis=1))
     return out
