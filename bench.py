@@ -337,6 +337,7 @@ def run_kvp(args):
     next_rows = {
         "kvpop_target": target_measure(kvp, x, plan, w, K, args.warmup, flush, peak, stream, dev),
         "ring_decode_step": ring_step_measure(kvp, dev, K, args.warmup, flush, peaks),
+        "kvpop_sparse_lse": sparse_lse_measure(kvp, x, w, K, args.warmup, flush, peak, stream, dev),
     }
 
     # end to end through the public API with host buffers
@@ -482,6 +483,43 @@ def target_measure(kvp, x, plan, w, K, W, flush, peak, stream, dev):
     return {"metric": "KVpop target pass TFLOP/s", "value": tf, "unit": "TFLOP/s",
             "frac": tf / peak, "ms": ms, "flops": flops, "aggregate": "max_log",
             "l2": "flushed before every launch"}
+
+
+def sparse_lse_measure(kvp, x, w, K, W, flush, peak, stream, dev):
+    """KVpop's running top-k sparse attention on the same layer: the cutoffs from seeded static
+    ranks (long-range budget k = budget - sinks - window), then the sparse row LSE.  The pass
+    scores every causal pair and masks per element, so its TFLOP/s counts the causal pairs."""
+    S, D = w.seq_len, w.head_dim
+    k_lr = w.budget - w.n_sink - w.window
+    ranks = kvp_inputs.make_static_ranks(w.h_kv, S, seed=3, device=dev)
+    tau = torch.empty_like(ranks)
+    lse = torch.empty(1, w.h_q, S, device=dev)
+
+    def run(ev=None):
+        if ev:
+            ev[0].record(stream)
+        kvp.kvp_topk_cutoffs(ranks, w.n_sink, w.window, k_lr, tau=tau)
+        if ev:
+            ev[1].record(stream)
+        kvp.kvp_sparse_lse_pass(x["q"], x["k"], ranks, tau, w.n_sink, w.window, lse=lse)
+        if ev:
+            ev[2].record(stream)
+
+    for _ in range(W):
+        run()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    for e in evs:
+        flush()
+        run(e)
+    torch.cuda.synchronize(dev)
+    kvp.kvp_check_device_status()
+    t_cut = sum(e[0].elapsed_time(e[1]) for e in evs) / K
+    t_lse = sum(e[1].elapsed_time(e[2]) for e in evs) / K
+    flops = 2.0 * D * w.h_q * (S * (S + 1) // 2)
+    tf = flops / (t_lse / 1e3) / 1e12
+    return {"metric": "sparse row LSE TFLOP/s (causal pairs)", "value": tf, "unit": "TFLOP/s",
+            "frac": tf / peak, "sparse_lse_ms": t_lse, "cutoffs_us": t_cut * 1e3,
+            "k_long_range": k_lr, "l2": "flushed before every pair of launches"}
 
 
 def ring_step_measure(kvp, dev, K, W, flush, peaks, cap=4096):

@@ -152,7 +152,7 @@ int kvp_future_attn_target(const void* q, const void* k, const float* lse, int d
  * tree; this library computes the same thresholds with per-chunk bitmaps.
  *
  * ranks [n_heads, seq_len] int32 (input), tau [n_heads, seq_len] int32 (output).
- * 1 <= seq_len <= 1048576, k >= 1, n_sink >= 0, window >= 0.  Ranks that are
+ * 1 <= seq_len <= 524288, k >= 1, n_sink >= 0, window >= 0.  Ranks that are
  * out of range or repeated are reported through the device status
  * (KVP_ERR_DEVICE_CHECK) and leave tau unspecified.
  * ------------------------------------------------------------------------- */

@@ -8,15 +8,17 @@
 // queries in order.  Here the same cutoffs come from a bitmap over the ranks, and the query
 // axis is cut into chunks that run in parallel:
 //
-//  * a CTA (head, chunk [q0, q1)) first sets the bits of every rank already eligible before
-//    q0 and finds the k-th smallest set bit with a block-wide count (word popcounts and a
-//    prefix sum over them);
-//  * one warp then walks the chunk's queries in order.  Inserting a rank above the cutoff
-//    changes nothing; inserting one below it moves the cutoff to the next set bit below the
-//    old cutoff (a ballot over 32 words at a time); when the k-th token arrives the cutoff is
-//    the largest set bit.
+//  * a CTA (head, chunk [q0, q0 + 512)) sets the bits of every rank already eligible before
+//    q0 (the static set A) and the per-word prefix counts of that bitmap;
+//  * each of its 8 warps walks 64 of the chunk's queries in order.  The set at query q is A
+//    plus the chunk's ranks inserted up to q (a short list with insertion order), so warps
+//    do not interfere.  A warp's first cutoff is found by a binary search on the rank axis
+//    (bitmap prefix count + a count over the list); then inserting a rank above the cutoff
+//    changes nothing, inserting one below it moves the cutoff to the largest member below
+//    the old cutoff (previous set bit of A, or the largest earlier list entry below it), and
+//    when the k-th token arrives the cutoff is the largest member.
 //
-// The output of the chunk is staged in shared memory and written with coalesced stores.
+// Repeated or out-of-range ranks are detected and reported through the device status.
 #include <climits>
 
 #include "kvp_common.cuh"
@@ -25,10 +27,12 @@
 namespace kvp {
 namespace {
 
-constexpr int CT_THREADS = 256;
-constexpr int CT_CHUNK = 512;     // queries per CTA
+constexpr int CT_WARPS = 8;
+constexpr int CT_THREADS = 32 * CT_WARPS;
+constexpr int CT_SUB = 64;                         // queries walked by one warp
+constexpr int CT_CHUNK = CT_WARPS * CT_SUB;        // queries per CTA
 
-// Largest set bit < limit (limit <= 32 * nw), or -1.  Warp-uniform result.
+// Largest set bit of the bitmap < limit, or -1 (warp-uniform).
 __device__ __forceinline__ int warp_prev_bit(const uint32_t* bits, int limit, int lane) {
   if (limit <= 0) return -1;
   const int w0 = (limit - 1) >> 5;
@@ -48,115 +52,152 @@ __device__ __forceinline__ int warp_prev_bit(const uint32_t* bits, int limit, in
   return -1;
 }
 
+// Largest list entry ins[j] < limit with j < n (entries < 0 are not ranks), or -1.
+__device__ __forceinline__ int warp_prev_listed(const int* ins, int n, int limit) {
+  int best = -1;
+  for (int j = threadIdx.x & 31; j < n; j += 32) {
+    const int r = ins[j];
+    if (r < limit && r > best) best = r;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
+  return best;
+}
+
+// Number of list entries 0 <= ins[j] <= x with j < n.
+__device__ __forceinline__ int warp_count_listed(const int* ins, int n, int x) {
+  int c = 0;
+  for (int j = threadIdx.x & 31; j < n; j += 32) {
+    const int r = ins[j];
+    c += (r >= 0 && r <= x) ? 1 : 0;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+  return c;
+}
+
 __global__ void __launch_bounds__(CT_THREADS) cutoff_kernel(const int32_t* __restrict__ ranks, int S,
                                                            int n_sink, int window, int k,
                                                            int32_t* __restrict__ tau, int* status) {
   extern __shared__ uint32_t sm[];
   const int nw = (S + 31) >> 5;
-  uint32_t* bits = sm;                                       // [nw]
-  int* cnt = reinterpret_cast<int*>(bits + nw);              // [CT_THREADS]
-  int* rk = cnt + CT_THREADS;                                // [CT_CHUNK] rank inserted at q (or -1)
-  int* out = rk + CT_CHUNK;                                  // [CT_CHUNK]
-  __shared__ int tau0_sh, bad_sh;
-  const int h = blockIdx.y, tid = threadIdx.x;
+  uint32_t* bits = sm;                                       // [nw] the static set A
+  int* wpre = reinterpret_cast<int*>(bits + nw);             // [nw] set bits in words before i
+  int* cnt = wpre + nw;                                      // [CT_THREADS]
+  int* ins = cnt + CT_THREADS;                               // [CT_CHUNK] rank inserted at q0 + i
+  int* out = ins + CT_CHUNK;                                 // [CT_CHUNK]
+  __shared__ int bad_sh, maxA_sh;
+  const int h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q0 = blockIdx.x * CT_CHUNK;
   if (q0 >= S) return;
   const int q1 = min(S, q0 + CT_CHUNK);
   const int32_t* rh = ranks + (size_t)h * S;
 
   for (int i = tid; i < nw; i += CT_THREADS) bits[i] = 0u;
-  if (tid == 0) {
-    tau0_sh = -1;
-    bad_sh = 0;
-  }
+  if (tid == 0) bad_sh = 0;
   __syncthreads();
-  // ranks eligible before q0: tokens s .. q0 - 1 - w
+  // A: ranks of tokens s .. q0 - 1 - w
   const long long t_last = (long long)q0 - 1 - window;
   int bad = 0;
   for (long long t = n_sink + tid; t <= t_last; t += CT_THREADS) {
     const int r = rh[t];
-    if ((unsigned)r < (unsigned)S) atomicOr(&bits[r >> 5], 1u << (r & 31));
-    else bad = 1;
+    if ((unsigned)r < (unsigned)S) {
+      const uint32_t bit = 1u << (r & 31);
+      if (atomicOr(&bits[r >> 5], bit) & bit) bad = 1;   // repeated rank
+    } else {
+      bad = 1;
+    }
   }
-  for (int q = q0 + tid; q < q1; q += CT_THREADS) {
-    const long long t = (long long)q - window;
-    int r = -1;
-    if (t >= n_sink) {
+  for (int i = tid; i < CT_CHUNK; i += CT_THREADS) {
+    const long long t = (long long)(q0 + i) - window;
+    int r = -1;                                              // no insert at this query
+    if (q0 + i < q1 && t >= n_sink) {
       r = rh[t];
       if ((unsigned)r >= (unsigned)S) {
         bad = 1;
-        r = -2;
+        r = -1;
       }
     }
-    rk[q - q0] = r;
+    ins[i] = r;
   }
+  __syncthreads();                                           // A is complete
+  // per-word prefix counts of A
+  const int per = (nw + CT_THREADS - 1) / CT_THREADS;
+  const int wa = min(nw, tid * per), wb = min(nw, wa + per);
+  int c = 0;
+  for (int i = wa; i < wb; ++i) c += __popc(bits[i]);
+  cnt[tid] = c;
+  __syncthreads();
+  for (int off = 1; off < CT_THREADS; off <<= 1) {            // inclusive scan (Hillis-Steele)
+    const int add = tid >= off ? cnt[tid - off] : 0;
+    __syncthreads();
+    cnt[tid] += add;
+    __syncthreads();
+  }
+  {
+    int run = tid ? cnt[tid - 1] : 0;
+    for (int i = wa; i < wb; ++i) {
+      wpre[i] = run;
+      run += __popc(bits[i]);
+    }
+  }
+  const long long e0 = t_last >= n_sink ? t_last - n_sink + 1 : 0;   // |A| if ranks are valid
+  if (tid == CT_THREADS - 1 && (long long)cnt[tid] != e0) bad = 1;
   if (bad) bad_sh = 1;
   __syncthreads();
-  const long long e0 = t_last >= n_sink ? t_last - n_sink + 1 : 0;   // eligible before q0
-
-  if (e0 > 0) {
-    // k-th smallest set bit: per-thread word ranges, popcount, exclusive prefix sum (the total
-    // also checks that the eligible ranks were distinct)
-    const int per = (nw + CT_THREADS - 1) / CT_THREADS;
-    const int wa = tid * per, wb = min(nw, wa + per);
-    int c = 0;
-    for (int i = wa; i < wb; ++i) c += __popc(bits[i]);
-    cnt[tid] = c;
-    __syncthreads();
-    for (int off = 1; off < CT_THREADS; off <<= 1) {          // inclusive scan (Hillis-Steele)
-      const int add = tid >= off ? cnt[tid - off] : 0;
-      __syncthreads();
-      cnt[tid] += add;
-      __syncthreads();
-    }
-    const int before = tid ? cnt[tid - 1] : 0;
-    if (tid == CT_THREADS - 1 && cnt[tid] != e0) bad_sh = 1;
-    if (e0 >= k && before < k && cnt[tid] >= k) {
-      int need = k - before;
-      for (int i = wa; i < wb; ++i) {
-        uint32_t v = bits[i];
-        const int pc = __popc(v);
-        if (need > pc) {
-          need -= pc;
-          continue;
-        }
-        for (int j = 1; j < need; ++j) v &= v - 1u;         // drop the need-1 lowest set bits
-        tau0_sh = (i << 5) + __ffs(v) - 1;
-        break;
-      }
-    }
-    __syncthreads();
-  }
-
-  if (tid < 32) {
-    const int lane = tid;
-    int cur = tau0_sh;
-    long long e = e0;
-    int err = 0;
-    for (int q = q0; q < q1; ++q) {
-      const int r = rk[q - q0];
-      if (r >= 0) {
-        const uint32_t bit = 1u << (r & 31);
-        const bool dup = (bits[r >> 5] & bit) != 0u;
-        __syncwarp();
-        if (lane == 0) bits[r >> 5] |= bit;
-        __syncwarp();
-        if (dup) {
-          err = 1;                                            // ranks are not a permutation
-        } else {
-          ++e;
-          if (e == k) cur = warp_prev_bit(bits, S, lane);     // largest eligible rank
-          else if (e > k && r < cur) cur = warp_prev_bit(bits, cur, lane);
-        }
-      } else if (r == -2) {
-        err = 1;
-      }
-      if (lane == 0) out[q - q0] = e >= k ? cur : -1;
-    }
-    if (lane == 0 && (err || bad_sh)) raise_status(status, KVP_ERR_DEVICE_CHECK);
+  if (warp == 0) {
+    const int m = warp_prev_bit(bits, S, lane);
+    if (lane == 0) maxA_sh = m;
   }
   __syncthreads();
-  for (int q = q0 + tid; q < q1; q += CT_THREADS) tau[(size_t)h * S + q] = out[q - q0];
+
+  // walk of this warp's queries [qa, qb)
+  const int ia = warp * CT_SUB, ib = min(q1 - q0, ia + CT_SUB);
+  if (ia < ib) {
+    int before = 0;                                          // inserts of the earlier warps
+    for (int j = lane; j < ia; j += 32) before += ins[j] >= 0 ? 1 : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+    long long e = e0 + before;
+    int cur = -1;
+    if (e >= k) {
+      // smallest x with |A <= x| + |list[0, ia) <= x| >= k
+      int lo = 0, hi = S - 1;
+      while (lo < hi) {
+        const int x = (lo + hi) >> 1;
+        const int wx = x >> 5, bx = x & 31;
+        const uint32_t upto = bx == 31 ? 0xffffffffu : ((2u << bx) - 1u);
+        const int cA = wpre[wx] + __popc(bits[wx] & upto);
+        if ((long long)cA + warp_count_listed(ins, ia, x) >= k) hi = x;
+        else lo = x + 1;
+      }
+      cur = lo;
+    }
+    for (int i = ia; i < ib; ++i) {
+      const int r = ins[i];
+      if (r >= 0) {
+        ++e;
+        if (e == k) {
+          cur = max(maxA_sh, warp_prev_listed(ins, i + 1, INT_MAX));
+        } else if (e > k && r < cur) {
+          cur = max(warp_prev_bit(bits, cur, lane), warp_prev_listed(ins, i + 1, cur));
+        }
+      }
+      if (lane == 0) out[i] = e >= k ? cur : -1;
+    }
+  }
+  __syncthreads();
+  // the chunk's ranks must be new and distinct
+  for (int i = tid; i < q1 - q0; i += CT_THREADS) {
+    const int r = ins[i];
+    if (r >= 0) {
+      const uint32_t bit = 1u << (r & 31);
+      if (atomicOr(&bits[r >> 5], bit) & bit) bad_sh = 1;
+    }
+    tau[(size_t)h * S + q0 + i] = out[i];
+  }
+  __syncthreads();
+  if (tid == 0 && bad_sh) raise_status(status, KVP_ERR_DEVICE_CHECK);
 }
 
 }  // namespace
@@ -164,7 +205,7 @@ __global__ void __launch_bounds__(CT_THREADS) cutoff_kernel(const int32_t* __res
 cudaError_t launch_topk_cutoffs(const int32_t* ranks, int n_heads, int S, int n_sink, int window,
                                 int k, int32_t* tau, int* status, cudaStream_t st) {
   const int nw = (S + 31) >> 5;
-  const size_t smem = ((size_t)nw + CT_THREADS + 2 * CT_CHUNK) * 4;
+  const size_t smem = (2 * (size_t)nw + CT_THREADS + 2 * CT_CHUNK) * 4;
   cudaError_t e = cudaFuncSetAttribute(cutoff_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((S + CT_CHUNK - 1) / CT_CHUNK, n_heads);

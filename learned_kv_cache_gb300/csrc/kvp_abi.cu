@@ -153,7 +153,7 @@ int kvp_topk_cutoffs(const int32_t* ranks, int n_heads, int seq_len, int n_sink,
   g_last_error.clear();
   if (!ranks || !tau) return fail(KVP_ERR_INVALID_ARG, "null ranks/tau");
   if (n_heads < 1 || n_heads > 65535) return fail(KVP_ERR_INVALID_ARG, "n_heads=%d", n_heads);
-  if (seq_len < 1 || seq_len > (1 << 20)) return fail(KVP_ERR_INVALID_ARG, "seq_len=%d", seq_len);
+  if (seq_len < 1 || seq_len > (1 << 19)) return fail(KVP_ERR_INVALID_ARG, "seq_len=%d", seq_len);
   if (k < 1) return fail(KVP_ERR_INVALID_ARG, "k=%d must be >= 1", k);
   if (n_sink < 0 || window < 0) return fail(KVP_ERR_INVALID_ARG, "n_sink=%d window=%d", n_sink, window);
   int* st = nullptr;
