@@ -70,6 +70,10 @@ constexpr int OFF_MISC = OFF_BAR + 256;
 constexpr int OFF_AEXT = OFF_MISC + 256;         // key-side extension: [1, 1, 1, 0, ...] per row
 constexpr int OFF_BEXT = OFF_AEXT + EXT_BYTES;   // query-side extension per stage: -lse/scale split
 constexpr int OFF_RED = OFF_BEXT + NSTAGE * EXT_BYTES;
+// Sparse LSE pass: ranks of the last NRK key tiles (the extension operands are unused there).
+constexpr int NRK = 8;
+constexpr int OFF_RANK = OFF_AEXT;
+static_assert(NRK * BN * 4 <= OFF_RED - OFF_AEXT, "rank ring must fit in the extension area");
 constexpr int SMEM_BYTES = OFF_RED + 2 * BM * 4 + 1024;   // + alignment slack
 
 // Byte offset of element (r, k) of a [128 x 16] K-major operand in 8 x 16-byte core matrices
@@ -204,6 +208,8 @@ __global__ void __launch_bounds__(THREADS, 2)
   const uint32_t bar_accf = bar_empty + 8 * NSTAGE;            // [NACC]
   const uint32_t bar_acce = bar_accf + 8 * NACC;               // [NACC]
   const uint32_t bar_a = bar_acce + 8 * NACC;
+  const uint32_t bar_rk = bar_a + 8;                           // [NRK] sparse LSE: ranks staged
+  int* rbuf = reinterpret_cast<int*>(smem + OFF_RANK);         // [NRK][BN]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
   float* red = reinterpret_cast<float*>(smem + OFF_RED);
@@ -223,6 +229,8 @@ __global__ void __launch_bounds__(THREADS, 2)
       ptx::mbar_init(bar_acce + 8 * a, EPI_WARPS);
     }
     ptx::mbar_init(bar_a, 1);
+    if (MODE == 2)
+      for (int b = 0; b < NRK; ++b) ptx::mbar_init(bar_rk + 8 * b, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -300,6 +308,25 @@ __global__ void __launch_bounds__(THREADS, 2)
       bool ok = true;
       if (use > 0) ok = ptx::mbar_wait(bar_empty + 8 * s, (use - 1) & 1, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, ok)) break;
+      if (MODE == 2) {
+        // Ranks of key tile t for the epilogue's mask.  Buffer t % NRK was last read for tile
+        // t - NRK; the wait above (MMA of tile t - 2 done, which itself waited for the
+        // epilogue to take tile t - 4 out of TMEM) keeps the epilogue past that tile.
+        const int kb = t * BN + 4 * lane;
+        const int32_t* src = p.ranks + (size_t)kv_z * p.S + kb;
+        int4 r4;
+        if (p.ranks_vec && kb + 3 < p.S) {
+          r4 = __ldg(reinterpret_cast<const int4*>(src));
+        } else {
+          r4.x = kb < p.S ? __ldg(src) : INT_MAX;
+          r4.y = kb + 1 < p.S ? __ldg(src + 1) : INT_MAX;
+          r4.z = kb + 2 < p.S ? __ldg(src + 2) : INT_MAX;
+          r4.w = kb + 3 < p.S ? __ldg(src + 3) : INT_MAX;
+        }
+        *reinterpret_cast<int4*>(rbuf + (t % NRK) * BN + 4 * lane) = r4;
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar_rk + 8 * (t % NRK));
+      }
       if (MODE == 1) {
         uint8_t* ext = smem + OFF_BEXT + s * EXT_BYTES;
 #pragma unroll
@@ -373,10 +400,8 @@ __global__ void __launch_bounds__(THREADS, 2)
     uint64_t acc01 = 0, acc23 = 0;                           // mass pass: packed fp32 pairs
     float m = -INFINITY, l = 0.f;                            // LSE pass running state
     const int row_i = it.tile * BM + r;                       // LSE passes: query of this row
-    const int32_t* ranks_row = nullptr;                      // sparse LSE: ranks of the KV head
     int tau_eff = INT_MAX;                                   // sparse LSE: cutoff (none: INT_MAX)
     if (MODE == 2) {
-      ranks_row = p.ranks + (size_t)kv_z * p.S;
       const int tq = row_i < p.S ? __ldg(p.tau + (size_t)kv_z * p.S + row_i) : -1;
       tau_eff = tq < 0 ? INT_MAX : tq;
     }
@@ -413,23 +438,31 @@ __global__ void __launch_bounds__(THREADS, 2)
           const int cw = row_i - p.window - jb, cs = p.n_sink - jb;
           const int lo = cs > 0 ? cs : 0, hi = cw < 63 ? cw : 63;
           if (__any_sync(0xffffffffu, tau_eff != INT_MAX && lo <= hi)) {
-            const int32_t* rk = ranks_row + jb;
-            if (p.ranks_vec && jb + 64 <= p.S) {
+            if (!ptx::mbar_wait(bar_rk + 8 * (t % NRK), (t / NRK) & 1, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            const int* rk = rbuf + (t % NRK) * BN + half * 64;
+            if (__all_sync(0xffffffffu, lo == 0 && hi == 63)) {
+              // every column eligible for every row of the warp: the rank test alone
 #pragma unroll
               for (int g4 = 0; g4 < 16; ++g4) {
-                const int4 r4 = __ldg(reinterpret_cast<const int4*>(rk) + g4);
+                const int4 r4 = *reinterpret_cast<const int4*>(rk + 4 * g4);
+                v[4 * g4 + 0] = r4.x > tau_eff ? 0xff800000u : v[4 * g4 + 0];
+                v[4 * g4 + 1] = r4.y > tau_eff ? 0xff800000u : v[4 * g4 + 1];
+                v[4 * g4 + 2] = r4.z > tau_eff ? 0xff800000u : v[4 * g4 + 2];
+                v[4 * g4 + 3] = r4.w > tau_eff ? 0xff800000u : v[4 * g4 + 3];
+              }
+            } else {
+#pragma unroll
+              for (int g4 = 0; g4 < 16; ++g4) {
+                const int4 r4 = *reinterpret_cast<const int4*>(rk + 4 * g4);
                 const int rr[4] = {r4.x, r4.y, r4.z, r4.w};
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                   const int c = 4 * g4 + u;
-                  if (c >= lo && c <= hi && rr[u] > tau_eff) v[c] = __float_as_uint(-INFINITY);
+                  if (c >= lo && c <= hi && rr[u] > tau_eff) v[c] = 0xff800000u;
                 }
-              }
-            } else {
-#pragma unroll
-              for (int c = 0; c < 64; ++c) {
-                if (c >= lo && c <= hi && jb + c < p.S && __ldg(rk + c) > tau_eff)
-                  v[c] = __float_as_uint(-INFINITY);
               }
             }
           }
