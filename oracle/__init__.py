@@ -16,6 +16,8 @@ Functions and the passages they follow:
 * :func:`decode_attn` -- How much KV cache can you prune, "Bounded windows".
 * :func:`ring_victim`, :func:`ring_insert` -- How much KV cache can you prune,
   "What we did" and "Conclusion" (static cache overwritten in place).
+* :func:`chunk_compress_step`, :func:`chunked_prefill_compress` -- Learning to Evict from
+  Key-Value Cache §4 and §4.1 (chunked prefill-compress with physical compaction).
 * :func:`fenwick_cutoffs`, :func:`sparse_mask`, :func:`sparse_row_lse` -- KVpop, "Efficient
   Online Pruning", "Fenwick-tree cut-off computation (Algorithm 2)" and "Delayed Memory
   Scoring" (the sparse log-normalisers).
@@ -29,6 +31,7 @@ pages' worked examples).
 from .attention_mass import future_attn_mass, future_attn_mass_per_head, kvpop_target, row_lse
 from .budgets import head_budgets, soft_topk
 from .decode import decode_attn
+from .chunked import chunk_compress_step, chunked_prefill_compress
 from .fenwick import fenwick_cutoffs, sparse_mask, sparse_row_lse
 from .ring import ring_insert, ring_victim
 from .selection import compact_kv, effective_budget, select_row, select_topk
@@ -36,5 +39,5 @@ from .selection import compact_kv, effective_budget, select_row, select_topk
 __all__ = [
     "row_lse", "future_attn_mass", "future_attn_mass_per_head", "kvpop_target", "select_topk", "select_row", "effective_budget",
     "compact_kv", "decode_attn", "soft_topk", "head_budgets", "ring_insert", "ring_victim",
-    "fenwick_cutoffs", "sparse_mask", "sparse_row_lse",
+    "fenwick_cutoffs", "sparse_mask", "sparse_row_lse", "chunk_compress_step", "chunked_prefill_compress",
 ]
