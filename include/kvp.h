@@ -12,6 +12,7 @@
  *
  * and the steps either side of them: kvp_future_attn_target (KVpop's supervision
  * target), kvp_ring_insert (in-place eviction of a static decode cache),
+ * kvp_chunk_compress (one step of chunked prefill-compress),
  * kvp_topk_cutoffs and kvp_sparse_lse_pass (KVpop's running top-k sparse
  * attention and its log-normalisers).
  *
@@ -236,6 +237,38 @@ int kvp_select_topk(const float* scores, int R, int T, int64_t row_stride,
 int kvp_compact_kv(const void* k, const void* v, int dtype, int R, int T, int head_dim,
                    const int32_t* idx, const int32_t* count, int b_max, void* k_out,
                    void* v_out, kvp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * A3'/A4''. One step of chunked prefill-compress.
+ *
+ * Learning to Evict from Key-Value Cache §4 and §4.1 (long contexts are
+ * prefilled chunk by chunk and the cache is compressed back to the budget
+ * after every chunk, with physical tensor compaction; budgets uniform across
+ * heads and layers) with the selection rule of kvp_select_topk (sinks, the
+ * most recent tokens and the top-scoring rest; scores are the per-token,
+ * query-agnostic ranking scores that stay with a token while it is kept):
+ *
+ *   union[r] = cache[r, 0 .. n_in) followed by chunk[r, 0 .. chunk_len)
+ *   kept     = kvp_select_topk(union scores, budget, n_sink, n_recent)
+ *   out[r, m] = union[r, idx[r, m]]  (K, V rows, score, source position)
+ *
+ * cache_k, cache_v [R, cap_in, head_dim] dtype; cache_score [R, cap_in] float32;
+ * cache_pos [R, cap_in] int32 (source positions): the previous step's output,
+ * n_in entries valid per row (n_in = 0: the first chunk; the cache pointers
+ * may then be null).  chunk_k, chunk_v [R, chunk_len, head_dim]; chunk_score
+ * [R, chunk_len]; the chunk's source positions are pos0 .. pos0+chunk_len-1.
+ * idx [R, out_cap] int32 (kept union indices, ascending, -1 padded) and
+ * count [R] int32 (kept per row: min(n_in + chunk_len, max(budget,
+ * n_sink + n_recent))) are outputs; so are out_k, out_v [R, out_cap,
+ * head_dim], out_score [R, out_cap], out_pos [R, out_cap] (the next step's
+ * cache; the output must not alias the inputs).  out_cap >= the kept count.
+ * ------------------------------------------------------------------------- */
+int kvp_chunk_compress(const void* cache_k, const void* cache_v, const float* cache_score,
+                       const int32_t* cache_pos, int cap_in, int n_in, const void* chunk_k,
+                       const void* chunk_v, const float* chunk_score, int chunk_len, int pos0,
+                       int dtype, int R, int head_dim, int budget, int n_sink, int n_recent,
+                       int32_t* idx, int32_t* count, void* out_k, void* out_v, float* out_score,
+                       int32_t* out_pos, int out_cap, kvp_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * A4'. In-place eviction of a static (ring) decode cache.

@@ -36,6 +36,8 @@ SIGNATURES = {
     "kvp_soft_topk_budgets": (_I, [_P, _I, _D, _I, _P, _P, _P]),
     "kvp_select_topk": (_I, [_P, _I, _I, _I64, _P, _I, _I, _P, _I, _P, _P]),
     "kvp_compact_kv": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P]),
+    "kvp_chunk_compress": (_I, [_P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P,
+                                _P, _P, _P, _P, _I, _P]),
     "kvp_ring_insert": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _I, _I, _P, _P]),
     "kvp_decode_attn_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "kvp_decode_attn": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _F, _P, _P, _P, _I, _I, _P,
@@ -311,6 +313,46 @@ def kvp_compact_kv(k, v, idx, count, k_out=None, v_out=None, stream=None):
                                _ptr(k_out), _ptr(v_out), _stream(stream))
     _check("kvp_compact_kv", rc)
     return k_out, v_out
+
+
+def kvp_chunk_compress(cache, n_in, chunk_k, chunk_v, chunk_score, pos0, budget, n_sink, n_recent,
+                       out, idx=None, count=None, stream=None):
+    """One chunked prefill-compress step.  ``cache`` and ``out`` are dicts of tensors "k", "v"
+    [R, cap, D], "score" float32 [R, cap] and "pos" int32 [R, cap] (``cache`` may be None when
+    n_in = 0).  Returns (idx, count)."""
+    _need(chunk_k, "chunk_k")
+    R, C, D = chunk_k.shape
+    _need(chunk_v, "chunk_v", chunk_k.dtype, (R, C, D))
+    _need(chunk_score, "chunk_score", torch.float32, (R, C))
+    out_cap = out["k"].shape[1]
+    _need(out["k"], "out k", chunk_k.dtype, (R, out_cap, D))
+    _need(out["v"], "out v", chunk_k.dtype, (R, out_cap, D))
+    _need(out["score"], "out score", torch.float32, (R, out_cap))
+    _need(out["pos"], "out pos", torch.int32, (R, out_cap))
+    if cache is not None:
+        cap_in = cache["k"].shape[1]
+        _need(cache["k"], "cache k", chunk_k.dtype, (R, cap_in, D))
+        _need(cache["v"], "cache v", chunk_k.dtype, (R, cap_in, D))
+        _need(cache["score"], "cache score", torch.float32, (R, cap_in))
+        _need(cache["pos"], "cache pos", torch.int32, (R, cap_in))
+        ck, cv, cs, cp = (_ptr(cache[x]) for x in ("k", "v", "score", "pos"))
+    else:
+        if n_in:
+            raise ValueError("n_in > 0 needs a cache")
+        cap_in, ck, cv, cs, cp = 0, None, None, None, None
+    if idx is None:
+        idx = torch.empty(R, out_cap, device=chunk_k.device, dtype=torch.int32)
+    if count is None:
+        count = torch.empty(R, device=chunk_k.device, dtype=torch.int32)
+    _need(idx, "idx", torch.int32, (R, out_cap))
+    _need(count, "count", torch.int32, (R,))
+    rc = load().kvp_chunk_compress(ck, cv, cs, cp, cap_in, int(n_in), _ptr(chunk_k), _ptr(chunk_v),
+                                   _ptr(chunk_score), C, int(pos0), _dtype(chunk_k), R, D, int(budget),
+                                   int(n_sink), int(n_recent), _ptr(idx), _ptr(count), _ptr(out["k"]),
+                                   _ptr(out["v"]), _ptr(out["score"]), _ptr(out["pos"]), out_cap,
+                                   _stream(stream))
+    _check("kvp_chunk_compress", rc)
+    return idx, count
 
 
 def kvp_ring_insert(kc, vc, slot_pos, slot_score, fill, new_k, new_v, new_pos, n_sink, n_recent,

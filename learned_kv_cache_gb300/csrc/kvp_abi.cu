@@ -5,6 +5,7 @@
 // stream; the library owns no memory except one int per device (the status
 // word that kernels use to report device-side range errors and bounded-wait
 // timeouts).
+#include <algorithm>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -318,6 +319,46 @@ int kvp_compact_kv(const void* k, const void* v, int dtype, int R, int T, int he
   cudaError_t e = kvp::launch_compact(k, v, head_dim * elem_size(dtype), R, T, idx, count, b_max,
                                       k_out, v_out, st, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "kvp_compact_kv launch");
+  return KVP_OK;
+}
+
+int kvp_chunk_compress(const void* cache_k, const void* cache_v, const float* cache_score,
+                       const int32_t* cache_pos, int cap_in, int n_in, const void* chunk_k,
+                       const void* chunk_v, const float* chunk_score, int chunk_len, int pos0,
+                       int dtype, int R, int head_dim, int budget, int n_sink, int n_recent,
+                       int32_t* idx, int32_t* count, void* out_k, void* out_v, float* out_score,
+                       int32_t* out_pos, int out_cap, kvp_stream_t stream) {
+  g_last_error.clear();
+  KVP_TRY(check_dtype(dtype));
+  if (!chunk_k || !chunk_v || !chunk_score || !idx || !count || !out_k || !out_v || !out_score || !out_pos)
+    return fail(KVP_ERR_INVALID_ARG, "null pointer");
+  if (n_in > 0 && (!cache_k || !cache_v || !cache_score || !cache_pos))
+    return fail(KVP_ERR_INVALID_ARG, "null cache pointer with n_in=%d", n_in);
+  if (R < 1 || chunk_len < 1 || n_in < 0 || n_in > cap_in)
+    return fail(KVP_ERR_INVALID_ARG, "R=%d chunk_len=%d n_in=%d cap_in=%d", R, chunk_len, n_in, cap_in);
+  if ((long long)n_in + chunk_len > 0x7fffffffLL) return fail(KVP_ERR_INVALID_ARG, "n_in + chunk_len overflows");
+  if (head_dim != 64 && head_dim != 128) return fail(KVP_ERR_UNSUPPORTED, "head_dim=%d", head_dim);
+  if (budget < 1 || n_sink < 0 || n_recent < 0)
+    return fail(KVP_ERR_INVALID_ARG, "budget=%d n_sink=%d n_recent=%d", budget, n_sink, n_recent);
+  if (pos0 < 0) return fail(KVP_ERR_INVALID_ARG, "pos0=%d < 0", pos0);
+  const int T = n_in + chunk_len;
+  const int b_eff = T <= budget ? T : std::min(T, std::max(budget, n_sink + n_recent));
+  if (out_cap < b_eff) return fail(KVP_ERR_INVALID_ARG, "out_cap=%d < kept count %d", out_cap, b_eff);
+  if ((n_in > 0 && (!aligned16(cache_k) || !aligned16(cache_v))) || !aligned16(chunk_k) ||
+      !aligned16(chunk_v) || !aligned16(out_k) || !aligned16(out_v))
+    return fail(KVP_ERR_INVALID_ARG, "K/V buffers not 16-byte aligned");
+  int* st = nullptr;
+  KVP_TRY(status_ptr(&st));
+  cudaError_t e = kvp::launch_select(n_in > 0 ? cache_score : chunk_score, R, T,
+                                     n_in > 0 ? (int64_t)cap_in : (int64_t)chunk_len, nullptr, n_sink,
+                                     n_recent, idx, out_cap, count, st, (cudaStream_t)stream,
+                                     n_in > 0 ? chunk_score : nullptr, chunk_len, n_in, budget);
+  if (e != cudaSuccess) return cuda_fail(e, "kvp_chunk_compress select launch");
+  const kvp::ChunkSrc src{cache_k, cache_v, cache_score, cache_pos, cap_in, n_in,
+                          chunk_k, chunk_v, chunk_score, chunk_len, pos0};
+  e = kvp::launch_chunk_compact(src, head_dim * elem_size(dtype), R, idx, count, out_cap, out_k, out_v,
+                                out_score, out_pos, out_cap, st, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kvp_chunk_compress compact launch");
   return KVP_OK;
 }
 

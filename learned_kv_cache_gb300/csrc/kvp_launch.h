@@ -45,12 +45,33 @@ cudaError_t launch_fam_tc(const void* q, const void* k, const float* lse, int dt
 
 cudaError_t launch_soft_topk(const double* x, int n, double k, int t, double* ratios,
                              int32_t* budgets, cudaStream_t st);
+// scores_b != null: the row is scores[0, n_a) followed by scores_b[0, T - n_a).
+// budgets == null: every row's budget is b_uniform.
 cudaError_t launch_select(const float* scores, int R, int T, int64_t row_stride,
                           const int32_t* budgets, int n_sink, int n_recent, int32_t* idx,
-                          int b_max, int32_t* count, int* status, cudaStream_t st);
+                          int b_max, int32_t* count, int* status, cudaStream_t st,
+                          const float* scores_b = nullptr, int64_t row_stride_b = 0, int n_a = 0,
+                          int b_uniform = 0);
 cudaError_t launch_compact(const void* k, const void* v, int row_bytes, int R, int T,
                            const int32_t* idx, const int32_t* count, int b_max, void* k_out,
                            void* v_out, int* status, cudaStream_t st);
+// Chunked prefill-compress: gather kept entries of [cache (n_in per row) ; chunk (C per row)]
+// -- K, V rows, scores and source positions -- into the output cache (row capacity out_cap).
+struct ChunkSrc {
+  const void* cache_k;
+  const void* cache_v;
+  const float* cache_score;
+  const int32_t* cache_pos;
+  int cap_in, n_in;
+  const void* chunk_k;
+  const void* chunk_v;
+  const float* chunk_score;
+  int C, pos0;
+};
+cudaError_t launch_chunk_compact(const ChunkSrc& src, int row_bytes, int R, const int32_t* idx,
+                                 const int32_t* count, int b_max, void* out_k, void* out_v,
+                                 float* out_score, int32_t* out_pos, int out_cap, int* status,
+                                 cudaStream_t st);
 
 // Running top-k cutoffs tau [n_heads, S] from static ranks (a permutation of 0..S-1 per head).
 cudaError_t launch_topk_cutoffs(const int32_t* ranks, int n_heads, int S, int n_sink, int window,

@@ -75,8 +75,13 @@ constexpr int SC_MAX_CLUSTER = 8;
 constexpr int SC_PRIV = 8;                // private histograms per CTA
 constexpr int SC_SMEM_KEYS = 16384;       // order keys of a slice held in shared memory (64 KB)
 
+// The scores of a row are entries 0..T-1 of the concatenation of two sources: positions
+// gi < n_a come from `scores` (row stride row_stride), the rest from `scores_b` (row stride
+// row_stride_b) at gi - n_a.  One source: n_a = T.  budgets == null: every row's budget is
+// b_uniform.
 __global__ void __launch_bounds__(SC_THREADS, 4) select_cluster_kernel(
-    const float* __restrict__ scores, int T, long long row_stride, const int32_t* __restrict__ budgets,
+    const float* __restrict__ scores, int T, long long row_stride, const float* __restrict__ scores_b,
+    long long row_stride_b, int n_a, const int32_t* __restrict__ budgets, int b_uniform,
     int n_sink, int n_recent, int32_t* __restrict__ idx, int b_max, int32_t* __restrict__ count,
     int* status) {
   namespace cg = cooperative_groups;
@@ -96,8 +101,10 @@ __global__ void __launch_bounds__(SC_THREADS, 4) select_cluster_kernel(
   const int tid = threadIdx.x;
 
   const float* s = scores + (size_t)r * row_stride;
+  const float* s_b = scores_b ? scores_b + (size_t)r * row_stride_b - n_a : nullptr;
+  auto score_at = [&](int gi) { return gi < n_a ? __ldg(s + gi) : __ldg(s_b + gi); };
   int32_t* out = idx + (size_t)r * b_max;
-  const int b = budgets[r];
+  const int b = budgets ? budgets[r] : b_uniform;
   const int b_eff = b < 0 ? -1 : ((T <= b) ? T : min(T, max(b, n_sink + n_recent)));
   if (b < 0 || b_eff > b_max) {          // every CTA of the cluster takes this exit
     if (rank == 0 && tid == 0) {
@@ -122,7 +129,7 @@ __global__ void __launch_bounds__(SC_THREADS, 4) select_cluster_kernel(
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int i = i0 + u * SC_THREADS + tid;
-        v[u] = i < nsm ? __ldg(s + lo + i) : 0.f;
+        v[u] = i < nsm ? score_at(lo + i) : 0.f;
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -132,7 +139,7 @@ __global__ void __launch_bounds__(SC_THREADS, 4) select_cluster_kernel(
     }
     __syncthreads();
   }
-  auto key_at = [&](int i) { return i < SC_SMEM_KEYS ? skeys[i] : order_key(__ldg(s + lo + i)); };
+  auto key_at = [&](int i) { return i < SC_SMEM_KEYS ? skeys[i] : order_key(score_at(lo + i)); };
   uint32_t prefix = 0u, mask = 0u;
   int remaining = k;
   if (k > 0) {
@@ -408,7 +415,8 @@ __global__ void __launch_bounds__(ST_THREADS) soft_topk_kernel(const double* __r
 
 cudaError_t launch_select(const float* scores, int R, int T, int64_t row_stride,
                           const int32_t* budgets, int n_sink, int n_recent, int32_t* idx,
-                          int b_max, int32_t* count, int* status, cudaStream_t st) {
+                          int b_max, int32_t* count, int* status, cudaStream_t st,
+                          const float* scores_b, int64_t row_stride_b, int n_a, int b_uniform) {
   int cl = 1;
   while (cl < SC_MAX_CLUSTER && T / (2 * cl) >= 1024) cl *= 2;
   const int per = (T + cl - 1) / cl;
@@ -430,7 +438,8 @@ cudaError_t launch_select(const float* scores, int R, int T, int64_t row_stride,
   cfg.numAttrs = 1;
   cudaError_t e;
   count_launches(1);
-  e = cudaLaunchKernelEx(&cfg, select_cluster_kernel, scores, T, (long long)row_stride, budgets, n_sink,
+  e = cudaLaunchKernelEx(&cfg, select_cluster_kernel, scores, T, (long long)row_stride, scores_b,
+                         (long long)row_stride_b, scores_b ? n_a : T, budgets, b_uniform, n_sink,
                          n_recent, idx, b_max, count, status);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
