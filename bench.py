@@ -338,6 +338,7 @@ def run_kvp(args):
         "kvpop_target": target_measure(kvp, x, plan, w, K, args.warmup, flush, peak, stream, dev),
         "ring_decode_step": ring_step_measure(kvp, dev, K, args.warmup, flush, peaks),
         "kvpop_sparse_lse": sparse_lse_measure(kvp, x, w, K, args.warmup, flush, peak, stream, dev),
+        "chunked_prefill_compress": chunked_measure(kvp, dev, args.warmup, flush, peaks),
     }
 
     # end to end through the public API with host buffers
@@ -520,6 +521,62 @@ def sparse_lse_measure(kvp, x, w, K, W, flush, peak, stream, dev):
     return {"metric": "sparse row LSE TFLOP/s (causal pairs)", "value": tf, "unit": "TFLOP/s",
             "frac": tf / peak, "sparse_lse_ms": t_lse, "cutoffs_us": t_cut * 1e3,
             "k_long_range": k_lr, "l2": "flushed before every pair of launches"}
+
+
+def chunked_measure(kvp, dev, W, flush, peaks, chunk=8192):
+    """Chunked prefill-compress on the Qwen2.5-1.5B cache shapes (56 rows, 120000 tokens, budget
+    4096, per-token static scores): the whole loop of compress steps, each timed with L2
+    flushed; reports the loop's time and the HBM rate of its K/V movement."""
+    w = kvp_inputs.QWEN25_15B_DECODE
+    x = kvp_inputs.make_decode_cache(w, device=dev)
+    R, T, D = w.rows, w.seq_len, w.head_dim
+    b = max(w.decode_budgets)
+    scores = kvp_inputs.make_scores(R, T, seed=7, device=dev)
+    chunks = [(p0, min(T, p0 + chunk)) for p0 in range(0, T, chunk)]
+    ck = [x["k"][:, a:e].contiguous() for a, e in chunks]
+    cv = [x["v"][:, a:e].contiguous() for a, e in chunks]
+    cs = [scores[:, a:e].contiguous() for a, e in chunks]
+    del x
+    bufs = [{"k": torch.empty(R, b, D, dtype=ck[0].dtype, device=dev),
+             "v": torch.empty(R, b, D, dtype=ck[0].dtype, device=dev),
+             "score": torch.empty(R, b, device=dev),
+             "pos": torch.empty(R, b, dtype=torch.int32, device=dev)} for _ in range(2)]
+    idx = torch.empty(R, b, dtype=torch.int32, device=dev)
+    cnt = torch.empty(R, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def loop(evs=None):
+        cache, n = None, 0
+        for i, (a, e) in enumerate(chunks):
+            if evs:
+                flush()
+                evs[i][0].record(stream)
+            out = bufs[i % 2]
+            kvp.kvp_chunk_compress(cache, n, ck[i], cv[i], cs[i], a, b, w.n_sink, w.n_recent, out,
+                                   idx=idx, count=cnt)
+            if evs:
+                evs[i][1].record(stream)
+            cache, n = out, min(max(b, w.n_sink + w.n_recent), n + (e - a))
+
+    for _ in range(W):
+        loop()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in chunks]
+    loop(evs)
+    torch.cuda.synchronize(dev)
+    kvp.kvp_check_device_status()
+    step_ms = [a.elapsed_time(e) for a, e in evs]
+    elt = ck[0].element_size()
+    moved, n = 0, 0
+    for a, e in chunks:
+        kept = min(max(b, w.n_sink + w.n_recent), n + (e - a))
+        moved += 2 * (2 * R * kept * D * elt) + R * (n + e - a) * 4 + R * kept * 12
+        n = kept
+    gbs = moved / (sum(step_ms) / 1e3) / 1e9
+    hbm = float(peaks["hbm_gbs"])
+    return {"metric": "chunked prefill-compress HBM GB/s", "value": gbs, "unit": "GB/s",
+            "frac": gbs / hbm, "peak": hbm, "loop_ms": sum(step_ms), "steps": len(chunks),
+            "chunk": chunk, "budget": b, "mean_step_us": sum(step_ms) / len(chunks) * 1e3,
+            "l2": "flushed before every step"}
 
 
 def ring_step_measure(kvp, dev, K, W, flush, peaks, cap=4096):
