@@ -12,7 +12,8 @@
  *
  * and the steps either side of them: kvp_future_attn_target (KVpop's supervision
  * target), kvp_ring_insert (in-place eviction of a static decode cache),
- * kvp_chunk_compress (one step of chunked prefill-compress),
+ * kvp_chunk_compress (one step of chunked prefill-compress), kvp_rank_rows and
+ * kvp_eviction_auc (static ranks; KVP's eviction-cost area of a ranking),
  * kvp_topk_cutoffs and kvp_sparse_lse_pass (KVpop's running top-k sparse
  * attention and its log-normalisers).
  *
@@ -180,6 +181,44 @@ int kvp_topk_cutoffs(const int32_t* ranks, int n_heads, int seq_len, int n_sink,
 int kvp_sparse_lse_pass(const void* q, const void* k, const int32_t* ranks, const int32_t* tau,
                         int dtype, int n_batch, int h_q, int h_kv, int seq_len, int head_dim,
                         float sm_scale, int n_sink, int window, float* lse, kvp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Ranks of score rows (static ranks; the optimal ranking of the eviction cost).
+ *
+ * KVpop, "Efficient Online Pruning" (tokens are pre-sorted by a static priority
+ * score and their ranks stored, for kvp_topk_cutoffs) and Learning to Evict
+ * from Key-Value Cache §3.1.1 (the optimal ranking orders entries by their
+ * importance):
+ *
+ *   ranks[r, t] = position of entry t when row r is sorted by score, highest
+ *                 first; equal scores in index order; NaN last; -0.0 == +0.0
+ *
+ * scores [R, T] float32, ranks [R, T] int32 (output, a permutation of 0..T-1
+ * per row).  workspace: kvp_rank_rows_workspace_size(R, T) bytes, 256-byte
+ * aligned (radix-sort buffers).  R <= 65535.
+ * ------------------------------------------------------------------------- */
+size_t kvp_rank_rows_workspace_size(int R, int T);
+int kvp_rank_rows(const float* scores, int R, int T, int32_t* ranks, void* workspace,
+                  size_t workspace_bytes, kvp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Eviction-cost area under the curve of a ranking (KVP's global reward).
+ *
+ * Learning to Evict from Key-Value Cache §1, §3 and §3.1.1: one ranking serves
+ * every budget b (entries of rank < b are kept); cost(b) is the importance of
+ * the entries it evicts, and the ranking is scored by the area under cost(b)
+ * over all budgets, normalised by the optimal ranking's area:
+ *
+ *   auc[r, m] = sum_{b=0}^{T} sum_{t : ranks[r,m,t] >= b} F[r, t]
+ *             = sum_t (ranks[r, m, t] + 1) * F[r, t]
+ *
+ * F [R, T] float32 (e.g. kvp_future_attn_mass's output), ranks [R, M, T] int32
+ * (M rankings per row, each taken as given), auc [R, M] float64 (output).  The
+ * normalised cost of a ranking is its auc divided by the auc of
+ * kvp_rank_rows(F).  R <= 65535.
+ * ------------------------------------------------------------------------- */
+int kvp_eviction_auc(const float* F, const int32_t* ranks, int R, int M, int T, double* auc,
+                     kvp_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * A0. Head-wise budgets from the closed-form Soft-TopK.

@@ -38,6 +38,9 @@ SIGNATURES = {
     "kvp_compact_kv": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P]),
     "kvp_chunk_compress": (_I, [_P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P,
                                 _P, _P, _P, _P, _I, _P]),
+    "kvp_rank_rows_workspace_size": (_SZ, [_I, _I]),
+    "kvp_rank_rows": (_I, [_P, _I, _I, _P, _P, _SZ, _P]),
+    "kvp_eviction_auc": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "kvp_ring_insert": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _I, _I, _P, _P]),
     "kvp_decode_attn_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "kvp_decode_attn": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _F, _P, _P, _P, _I, _I, _P,
@@ -353,6 +356,40 @@ def kvp_chunk_compress(cache, n_in, chunk_k, chunk_v, chunk_score, pos0, budget,
                                    _stream(stream))
     _check("kvp_chunk_compress", rc)
     return idx, count
+
+
+def kvp_rank_rows(scores, ranks=None, workspace=None, stream=None):
+    """scores float32 [..., T] (one row per leading index) -> ranks int32 of the same shape."""
+    _need(scores, "scores", torch.float32)
+    T = scores.shape[-1]
+    R = scores.numel() // max(T, 1)
+    if ranks is None:
+        ranks = torch.empty(scores.shape, device=scores.device, dtype=torch.int32)
+    _need(ranks, "ranks", torch.int32, tuple(scores.shape))
+    need = int(load().kvp_rank_rows_workspace_size(R, T))
+    if workspace is None:
+        workspace = torch.empty(need, device=scores.device, dtype=torch.uint8)
+    rc = load().kvp_rank_rows(_ptr(scores), R, T, _ptr(ranks), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("kvp_rank_rows", rc)
+    return ranks
+
+
+def kvp_eviction_auc(F, ranks, auc=None, stream=None):
+    """F float32 [R, T], ranks int32 [R, M, T] (or [R, T] for M = 1) -> auc float64 [R, M]."""
+    _need(F, "F", torch.float32)
+    R, T = F.shape
+    r3 = ranks if ranks.dim() == 3 else ranks.unsqueeze(1)
+    _need(r3, "ranks", torch.int32)
+    if r3.shape[0] != R or r3.shape[2] != T:
+        raise ValueError("ranks must be [R, M, T]")
+    M = r3.shape[1]
+    if auc is None:
+        auc = torch.empty(R, M, device=F.device, dtype=torch.float64)
+    _need(auc, "auc", torch.float64, (R, M))
+    rc = load().kvp_eviction_auc(_ptr(F), _ptr(r3), R, M, T, _ptr(auc), _stream(stream))
+    _check("kvp_eviction_auc", rc)
+    return auc
 
 
 def kvp_ring_insert(kc, vc, slot_pos, slot_score, fill, new_k, new_v, new_pos, n_sink, n_recent,

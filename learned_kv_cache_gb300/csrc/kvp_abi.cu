@@ -362,6 +362,37 @@ int kvp_chunk_compress(const void* cache_k, const void* cache_v, const float* ca
   return KVP_OK;
 }
 
+size_t kvp_rank_rows_workspace_size(int R, int T) {
+  if (R < 1 || R > 65535 || T < 1) return 0;
+  return kvp::rank_rows_workspace_size(R, T);
+}
+
+int kvp_rank_rows(const float* scores, int R, int T, int32_t* ranks, void* workspace,
+                  size_t workspace_bytes, kvp_stream_t stream) {
+  g_last_error.clear();
+  if (!scores || !ranks) return fail(KVP_ERR_INVALID_ARG, "null scores/ranks");
+  if (R < 1 || R > 65535 || T < 1) return fail(KVP_ERR_INVALID_ARG, "R=%d T=%d", R, T);
+  const size_t need = kvp::rank_rows_workspace_size(R, T);
+  if (!workspace || workspace_bytes < need)
+    return fail(KVP_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+  if (((uintptr_t)workspace & 255) != 0) return fail(KVP_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+  int* st = nullptr;
+  KVP_TRY(status_ptr(&st));
+  cudaError_t e = kvp::launch_rank_rows(scores, R, T, ranks, workspace, st, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kvp_rank_rows launch");
+  return KVP_OK;
+}
+
+int kvp_eviction_auc(const float* F, const int32_t* ranks, int R, int M, int T, double* auc,
+                     kvp_stream_t stream) {
+  g_last_error.clear();
+  if (!F || !ranks || !auc) return fail(KVP_ERR_INVALID_ARG, "null F/ranks/auc");
+  if (R < 1 || R > 65535 || M < 1 || T < 1) return fail(KVP_ERR_INVALID_ARG, "R=%d M=%d T=%d", R, M, T);
+  cudaError_t e = kvp::launch_eviction_auc(F, ranks, R, M, T, auc, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kvp_eviction_auc launch");
+  return KVP_OK;
+}
+
 int kvp_ring_insert(void* kc, void* vc, int32_t* slot_pos, float* slot_score, int32_t* fill,
                     int dtype, int R, int cap, int head_dim, const void* new_k, const void* new_v,
                     int new_pos, int n_sink, int n_recent, int32_t* out_slot, kvp_stream_t stream) {

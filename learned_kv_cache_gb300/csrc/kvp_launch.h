@@ -77,6 +77,14 @@ cudaError_t launch_chunk_compact(const ChunkSrc& src, int row_bytes, int R, cons
 cudaError_t launch_topk_cutoffs(const int32_t* ranks, int n_heads, int S, int n_sink, int window,
                                 int k, int32_t* tau, int* status, cudaStream_t st);
 
+// Per-row ranks of scores (0 = highest, ties to the lower index, NaN last) and the
+// eviction-cost AUC sum_t (rank_t + 1) * F_t of M rankings per row.
+size_t rank_rows_workspace_size(int R, int T);
+cudaError_t launch_rank_rows(const float* scores, int R, int T, int32_t* ranks, void* ws,
+                             int* status, cudaStream_t st);
+cudaError_t launch_eviction_auc(const float* F, const int32_t* ranks, int R, int M, int T,
+                                double* auc, cudaStream_t st);
+
 cudaError_t launch_ring_insert(void* kc, void* vc, int32_t* slot_pos, float* slot_score, int32_t* fill,
                                int R, int cap, int row_bytes, const void* new_k, const void* new_v,
                                int new_pos, int n_sink, int n_recent, int32_t* out_slot, int* status,
