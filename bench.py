@@ -339,6 +339,7 @@ def run_kvp(args):
         "ring_decode_step": ring_step_measure(kvp, dev, K, args.warmup, flush, peaks),
         "kvpop_sparse_lse": sparse_lse_measure(kvp, x, w, K, args.warmup, flush, peak, stream, dev),
         "chunked_prefill_compress": chunked_measure(kvp, dev, args.warmup, flush, peaks),
+        "kvp_eviction_auc": rank_auc_measure(kvp, dev, args.warmup, min(K, 20), flush, peaks),
     }
 
     # end to end through the public API with host buffers
@@ -577,6 +578,47 @@ def chunked_measure(kvp, dev, W, flush, peaks, chunk=8192):
             "frac": gbs / hbm, "peak": hbm, "loop_ms": sum(step_ms), "steps": len(chunks),
             "chunk": chunk, "budget": b, "mean_step_us": sum(step_ms) / len(chunks) * 1e3,
             "l2": "flushed before every step"}
+
+
+def rank_auc_measure(kvp, dev, W, K, flush, peaks, M=16):
+    """Qwen3-8B 131k shapes (8 KV heads x 131072 tokens): static ranks from scores (the ranking
+    sort) and the eviction-cost AUC of M rankings per head, each timed with L2 flushed."""
+    w = kvp_inputs.QWEN3_8B_131K
+    R, T = w.h_kv, w.seq_len
+    s = kvp_inputs.make_scores(R, T, seed=21, device=dev)
+    ranks = torch.empty(R, T, dtype=torch.int32, device=dev)
+    ws = torch.empty(int(kvp.load().kvp_rank_rows_workspace_size(R, T)), dtype=torch.uint8, device=dev)
+    F = torch.rand(R, T, generator=torch.Generator(device=dev).manual_seed(4), device=dev)
+    many = torch.stack([torch.randperm(T, device=dev) for _ in range(R * M)]).view(R, M, T).to(torch.int32)
+    auc = torch.empty(R, M, dtype=torch.float64, device=dev)
+    aws = torch.empty(int(kvp.load().kvp_eviction_auc_workspace_size(R, M, T)), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(W):
+        kvp.kvp_rank_rows(s, ranks=ranks, workspace=ws)
+        kvp.kvp_eviction_auc(F, many, auc=auc, workspace=aws)
+    t_rank, t_auc = [], []
+    for _ in range(K):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        flush()
+        e[0].record(stream)
+        kvp.kvp_rank_rows(s, ranks=ranks, workspace=ws)
+        e[1].record(stream)
+        flush()
+        e[2].record(stream)
+        kvp.kvp_eviction_auc(F, many, auc=auc, workspace=aws)
+        e[3].record(stream)
+        torch.cuda.synchronize(dev)
+        t_rank.append(e[0].elapsed_time(e[1]))
+        t_auc.append(e[2].elapsed_time(e[3]))
+    kvp.kvp_check_device_status()
+    ms_r, ms_a = sum(t_rank) / K, sum(t_auc) / K
+    rank_bytes = 4 * (2 * R * T * 8) + R * T * 8          # four passes of (key, index) read+write, scores, ranks
+    auc_bytes = R * M * T * 4 + R * T * 4
+    hbm = float(peaks["hbm_gbs"])
+    return {"metric": "eviction-cost AUC HBM GB/s", "value": auc_bytes / (ms_a / 1e3) / 1e9, "unit": "GB/s",
+            "frac": auc_bytes / (ms_a / 1e3) / 1e9 / hbm, "auc_ms": ms_a, "rankings": M,
+            "rank_rows_ms": ms_r, "rank_rows_GB/s": rank_bytes / (ms_r / 1e3) / 1e9,
+            "rows": R, "T": T, "l2": "flushed before every launch"}
 
 
 def ring_step_measure(kvp, dev, K, W, flush, peaks, cap=4096):

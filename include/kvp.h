@@ -215,10 +215,13 @@ int kvp_rank_rows(const float* scores, int R, int T, int32_t* ranks, void* works
  * F [R, T] float32 (e.g. kvp_future_attn_mass's output), ranks [R, M, T] int32
  * (M rankings per row, each taken as given), auc [R, M] float64 (output).  The
  * normalised cost of a ranking is its auc divided by the auc of
- * kvp_rank_rows(F).  R <= 65535.
+ * kvp_rank_rows(F).  Products and sums are exact to fp64 rounding.
+ * workspace: kvp_eviction_auc_workspace_size(R, M, T) bytes (per-chunk partial
+ * sums, added in fixed order).  R, M <= 65535.
  * ------------------------------------------------------------------------- */
+size_t kvp_eviction_auc_workspace_size(int R, int M, int T);
 int kvp_eviction_auc(const float* F, const int32_t* ranks, int R, int M, int T, double* auc,
-                     kvp_stream_t stream);
+                     void* workspace, size_t workspace_bytes, kvp_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * A0. Head-wise budgets from the closed-form Soft-TopK.

@@ -40,7 +40,8 @@ SIGNATURES = {
                                 _P, _P, _P, _P, _I, _P]),
     "kvp_rank_rows_workspace_size": (_SZ, [_I, _I]),
     "kvp_rank_rows": (_I, [_P, _I, _I, _P, _P, _SZ, _P]),
-    "kvp_eviction_auc": (_I, [_P, _P, _I, _I, _I, _P, _P]),
+    "kvp_eviction_auc_workspace_size": (_SZ, [_I, _I, _I]),
+    "kvp_eviction_auc": (_I, [_P, _P, _I, _I, _I, _P, _P, _SZ, _P]),
     "kvp_ring_insert": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _I, _I, _P, _P]),
     "kvp_decode_attn_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "kvp_decode_attn": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _F, _P, _P, _P, _I, _I, _P,
@@ -375,7 +376,7 @@ def kvp_rank_rows(scores, ranks=None, workspace=None, stream=None):
     return ranks
 
 
-def kvp_eviction_auc(F, ranks, auc=None, stream=None):
+def kvp_eviction_auc(F, ranks, auc=None, workspace=None, stream=None):
     """F float32 [R, T], ranks int32 [R, M, T] (or [R, T] for M = 1) -> auc float64 [R, M]."""
     _need(F, "F", torch.float32)
     R, T = F.shape
@@ -387,7 +388,11 @@ def kvp_eviction_auc(F, ranks, auc=None, stream=None):
     if auc is None:
         auc = torch.empty(R, M, device=F.device, dtype=torch.float64)
     _need(auc, "auc", torch.float64, (R, M))
-    rc = load().kvp_eviction_auc(_ptr(F), _ptr(r3), R, M, T, _ptr(auc), _stream(stream))
+    need = int(load().kvp_eviction_auc_workspace_size(R, M, T))
+    if workspace is None:
+        workspace = torch.empty(need, device=F.device, dtype=torch.uint8)
+    rc = load().kvp_eviction_auc(_ptr(F), _ptr(r3), R, M, T, _ptr(auc), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream))
     _check("kvp_eviction_auc", rc)
     return auc
 

@@ -383,12 +383,22 @@ int kvp_rank_rows(const float* scores, int R, int T, int32_t* ranks, void* works
   return KVP_OK;
 }
 
+size_t kvp_eviction_auc_workspace_size(int R, int M, int T) {
+  if (R < 1 || R > 65535 || M < 1 || M > 65535 || T < 1) return 0;
+  return kvp::eviction_auc_workspace_size(R, M, T);
+}
+
 int kvp_eviction_auc(const float* F, const int32_t* ranks, int R, int M, int T, double* auc,
-                     kvp_stream_t stream) {
+                     void* workspace, size_t workspace_bytes, kvp_stream_t stream) {
   g_last_error.clear();
   if (!F || !ranks || !auc) return fail(KVP_ERR_INVALID_ARG, "null F/ranks/auc");
-  if (R < 1 || R > 65535 || M < 1 || T < 1) return fail(KVP_ERR_INVALID_ARG, "R=%d M=%d T=%d", R, M, T);
-  cudaError_t e = kvp::launch_eviction_auc(F, ranks, R, M, T, auc, (cudaStream_t)stream);
+  if (R < 1 || R > 65535 || M < 1 || M > 65535 || T < 1)
+    return fail(KVP_ERR_INVALID_ARG, "R=%d M=%d T=%d", R, M, T);
+  const size_t need = kvp::eviction_auc_workspace_size(R, M, T);
+  if (!workspace || workspace_bytes < need)
+    return fail(KVP_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+  if (((uintptr_t)workspace & 7) != 0) return fail(KVP_ERR_INVALID_ARG, "workspace not 8-byte aligned");
+  cudaError_t e = kvp::launch_eviction_auc(F, ranks, R, M, T, auc, workspace, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "kvp_eviction_auc launch");
   return KVP_OK;
 }

@@ -82,8 +82,9 @@ cudaError_t launch_topk_cutoffs(const int32_t* ranks, int n_heads, int S, int n_
 size_t rank_rows_workspace_size(int R, int T);
 cudaError_t launch_rank_rows(const float* scores, int R, int T, int32_t* ranks, void* ws,
                              int* status, cudaStream_t st);
+size_t eviction_auc_workspace_size(int R, int M, int T);
 cudaError_t launch_eviction_auc(const float* F, const int32_t* ranks, int R, int M, int T,
-                                double* auc, cudaStream_t st);
+                                double* auc, void* ws, cudaStream_t st);
 
 cudaError_t launch_ring_insert(void* kc, void* vc, int32_t* slot_pos, float* slot_score, int32_t* fill,
                                int R, int cap, int row_bytes, const void* new_k, const void* new_v,

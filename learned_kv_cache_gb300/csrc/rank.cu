@@ -136,25 +136,74 @@ __global__ void rank_invert_kernel(const int32_t* __restrict__ vals, int R, int 
   }
 }
 
-// auc[r, m] = sum_t (ranks[r, m, t] + 1) * F[r, t]
-__global__ void __launch_bounds__(256) auc_kernel(const float* __restrict__ F,
-                                                  const int32_t* __restrict__ ranks, int M, int T,
-                                                  double* __restrict__ auc) {
-  __shared__ double red[256 / 32];
-  const int m = blockIdx.x, r = blockIdx.y, tid = threadIdx.x;
+// auc[r, m] = sum_t (ranks[r, m, t] + 1) * F[r, t], in two kernels: partial sums over chunks
+// of AUC_CHUNK entries (grid chunk x ranking x row), then a fixed-order sum of the partials.
+// Each product (rank + 1) * F is split exactly into two fp32 numbers (product and its FMA
+// residual; rank + 1 <= 2^24 is exact in fp32) and the terms are added with a compensated
+// (two-sum) fp32 pair, so the fp64 result carries no product rounding and no long-sum drift.
+constexpr int AUC_THREADS = 256;
+constexpr int AUC_CHUNK = 8192;
+
+__device__ __forceinline__ void two_sum_add(float& hi, float& lo, float x) {
+  const float s = hi + x;
+  const float bp = s - hi;
+  const float err = (hi - (s - bp)) + (x - bp);
+  hi = s;
+  lo += err;
+}
+
+__global__ void __launch_bounds__(AUC_THREADS) auc_partial_kernel(const float* __restrict__ F,
+                                                                  const int32_t* __restrict__ ranks,
+                                                                  int M, int T, int NC, int vec,
+                                                                  double* __restrict__ part) {
+  __shared__ double red[AUC_THREADS / 32];
+  const int c = blockIdx.x, m = blockIdx.y, r = blockIdx.z, tid = threadIdx.x;
   const float* f = F + (size_t)r * T;
   const int32_t* rk = ranks + ((size_t)r * M + m) * T;
-  double acc = 0.0;
-  for (int t = tid; t < T; t += 256) acc = fma((double)rk[t] + 1.0, (double)f[t], acc);   // exact products
+  const int t0 = c * AUC_CHUNK, t1 = min(T, t0 + AUC_CHUNK);
+  float hi = 0.f, lo = 0.f;
+  auto add = [&](int rank, float fv) {
+    const float a = (float)(rank + 1);
+    const float p = a * fv;
+    const float e = fmaf(a, fv, -p);          // a * fv = p + e exactly
+    two_sum_add(hi, lo, p);
+    lo += e;
+  };
+  if (vec) {                                   // rows 16-byte aligned: 4 entries per load
+    for (int t = t0 + 4 * tid; t < t1; t += 4 * AUC_THREADS) {
+      if (t + 3 < t1) {
+        const int4 r4 = __ldg(reinterpret_cast<const int4*>(rk + t));
+        const float4 f4 = __ldg(reinterpret_cast<const float4*>(f + t));
+        add(r4.x, f4.x);
+        add(r4.y, f4.y);
+        add(r4.z, f4.z);
+        add(r4.w, f4.w);
+      } else {
+        for (int u = t; u < t1; ++u) add(__ldg(rk + u), __ldg(f + u));
+      }
+    }
+  } else {
+    for (int t = t0 + tid; t < t1; t += AUC_THREADS) add(__ldg(rk + t), __ldg(f + t));
+  }
+  double acc = (double)hi + (double)lo;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   if ((tid & 31) == 0) red[tid >> 5] = acc;
   __syncthreads();
   if (tid == 0) {
     double s = 0.0;
-    for (int w = 0; w < 256 / 32; ++w) s += red[w];
-    auc[(size_t)r * M + m] = s;
+    for (int w = 0; w < AUC_THREADS / 32; ++w) s += red[w];
+    part[((size_t)r * M + m) * NC + c] = s;
   }
+}
+
+__global__ void auc_reduce_kernel(const double* __restrict__ part, int RM, int NC,
+                                  double* __restrict__ auc) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= RM) return;
+  double s = 0.0;
+  for (int c = 0; c < NC; ++c) s += part[(size_t)i * NC + c];
+  auc[i] = s;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -203,10 +252,20 @@ cudaError_t launch_rank_rows(const float* scores, int R, int T, int32_t* ranks, 
   return cudaGetLastError();
 }
 
+size_t eviction_auc_workspace_size(int R, int M, int T) {
+  const int NC = (T + AUC_CHUNK - 1) / AUC_CHUNK;
+  return align256((size_t)R * M * NC * sizeof(double));
+}
+
 cudaError_t launch_eviction_auc(const float* F, const int32_t* ranks, int R, int M, int T,
-                                double* auc, cudaStream_t st) {
-  count_launches(1);
-  auc_kernel<<<dim3(M, R), 256, 0, st>>>(F, ranks, M, T, auc);
+                                double* auc, void* ws, cudaStream_t st) {
+  const int NC = (T + AUC_CHUNK - 1) / AUC_CHUNK;
+  const int vec = T % 4 == 0 && ((uintptr_t)F & 15) == 0 && ((uintptr_t)ranks & 15) == 0;
+  double* part = (double*)ws;
+  count_launches(2);
+  auc_partial_kernel<<<dim3(NC, M, R), AUC_THREADS, 0, st>>>(F, ranks, M, T, NC, vec, part);
+  const int RM = R * M;
+  auc_reduce_kernel<<<(RM + 255) / 256, 256, 0, st>>>(part, RM, NC, auc);
   return cudaGetLastError();
 }
 
