@@ -44,9 +44,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic of one launch of the dominant kernel from an ncu capture, valid only while the
 # kernel source is unchanged (sha256 of the .cu file at capture time).
 NCU_TRAFFIC = {
-    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on this bench command, launches 7-10
-    # (profiles/traffic_bench_step.md): 117.24 / 116.44 MB read + 0.32 / 0.23 MB written
-    "future_attn_mass": {"sha": "901c9dcf0bcea0f1", "bytes": int((117244160 + 116442368 + 318208 + 226560) / 2)},
+    # ncu --set full of attn_tc_kernel<1> on the benchmark layer (S = 8192; the kernel source hashed
+    # below): 115.28 MB read + 3.61 MB written per launch (profiles/attn_tc_fam_qwen3-4b-layer_S8192.md)
+    "future_attn_mass": {"sha": "a7e88300ec2fd2a9", "bytes": 115278848 + 3609088},
 }
 
 
@@ -722,8 +722,8 @@ def e2e_measure(kvp, x, plan, budgets, w, K, W, stream, flops, ws, dev):
 
 def run_ncu_case(args):
     """A fixed case for profiler captures: `--steps` launches of one stage, no timing.
-    lse / fam: one Qwen3-4B-shaped layer at --seq-len (default 32768: Q = 256 MiB, larger than
-    L2); decode / select / compact / ring: the Qwen2.5-1.5B decode-eviction shapes (T = 120000,
+    lse / fam / sparse (cutoffs + sparse LSE): one Qwen3-4B-shaped layer at --seq-len (default
+    32768: Q = 256 MiB, larger than L2); decode / select / compact / ring: the Qwen2.5-1.5B decode-eviction shapes (T = 120000,
     28 layers x 2 KV heads, budget 4096; ring: a full static cache of 4096 slots per row, one
     insert plus one decode with accumulated key mass per step)."""
     import learned_kv_cache_gb300 as kvp
@@ -731,17 +731,24 @@ def run_ncu_case(args):
     torch.cuda.set_device(dev)
     kvp.load()
     case = args.ncu_case
-    if case in ("lse", "fam"):
+    if case in ("lse", "fam", "sparse"):
         w = kvp_inputs.QWEN3_4B_LAYER.scaled(seq_len=args.seq_len)
         x = kvp_inputs.make_prefill_layer(w, 0, device=dev)
         q, k = x["q"][None].contiguous(), x["k"][None].contiguous()
         lse = kvp.kvp_lse_pass(q, k)
         F = kvp.kvp_future_attn_mass(q, k, lse, w.window)
+        if case == "sparse":
+            k_lr = w.budget - w.n_sink - w.window
+            ranks = kvp_inputs.make_static_ranks(w.h_kv, w.seq_len, seed=3, device=dev)
+            tau = kvp.kvp_topk_cutoffs(ranks, w.n_sink, w.window, k_lr)
         for _ in range(args.steps):
             if case == "lse":
                 kvp.kvp_lse_pass(q, k, lse=lse)
-            else:
+            elif case == "fam":
                 kvp.kvp_future_attn_mass(q, k, lse, w.window, F=F)
+            else:
+                kvp.kvp_topk_cutoffs(ranks, w.n_sink, w.window, k_lr, tau=tau)
+                kvp.kvp_sparse_lse_pass(q, k, ranks, tau, w.n_sink, w.window, lse=lse)
     else:
         w = kvp_inputs.QWEN25_15B_DECODE
         R, T, D, b = w.rows, w.seq_len, w.head_dim, max(w.decode_budgets)
