@@ -680,30 +680,18 @@ def ring_step_measure(kvp, dev, K, W, flush, peaks, cap=4096):
 
 
 def e2e_measure(kvp, x, plan, budgets, w, K, W, stream, flops, ws, dev):
-    """Whole step through the public API from pinned host buffers: H2D of Q/K/V and the decode
-    query, the five stages, D2H of F, the kept indices/counts and the decode output."""
-    R, S, D = w.rows, w.seq_len, w.head_dim
+    """Whole step through the public API from pinned host buffers
+    (PrefillPrunePlan.run_from_host): H2D of Q/K/V and the decode query in four KV-head slices,
+    overlapped with the slices' LSE and mass passes, then selection, compaction, decode and the
+    D2H of F, the kept indices/counts and the decode output."""
     host = {k: v.cpu().pin_memory() for k, v in x.items()}
-    dx = {k: torch.empty_like(v) for k, v in x.items()}
     outs = {"F": plan.F, "idx": plan.idx, "count": plan.count, "out": plan.out}
     host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
 
     def step():
-        for k in dx:
-            dx[k].copy_(host[k], non_blocking=True)
-        kvp.kvp_lse_pass(dx["q"], dx["k"], lse=plan.lse)
-        kvp.kvp_future_attn_mass(dx["q"], dx["k"], plan.lse, w.window, F=plan.F,
-                                 workspace=plan.fam_ws)
-        kvp.kvp_select_topk(plan.F.view(R, S), budgets, w.n_sink, w.n_recent, w.budget,
-                            idx=plan.idx, count=plan.count)
-        kvp.kvp_compact_kv(dx["k"].view(R, S, D), dx["v"].view(R, S, D), plan.idx, plan.count,
-                           k_out=plan.kc, v_out=plan.vc)
-        kvp.kvp_decode_attn(dx["dq"], plan.kc, plan.vc, plan.count, out=plan.out,
-                            workspace=plan.dec_ws)
-        for k in outs:
-            host_out[k].copy_(outs[k], non_blocking=True)
+        plan.run_from_host(host["q"], host["k"], host["v"], host["dq"], budgets, host_out, stream=stream)
 
     for _ in range(W):
         step()
@@ -715,9 +703,11 @@ def e2e_measure(kvp, x, plan, budgets, w, K, W, stream, flops, ws, dev):
         step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
+    kvp.kvp_check_device_status()
     ms = e0.elapsed_time(e1) / K
     return {"value": flops * ws / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "overlap": "H2D in four KV-head slices on a copy stream; each slice's LSE pass starts when it lands, its mass pass on a second compute stream"}
 
 
 def run_ncu_case(args):
