@@ -19,9 +19,7 @@
 //    head of the GQA group; each TMEM lane is one key row and simply
 //    accumulates exp2(s*log2e*scale - lse_i*log2e) over its columns, so the
 //    column sums of the attention matrix become per-thread row sums with no
-//    atomics; the producer warp stages -lse_i*log2e of each query tile in
-//    shared memory (a ring of 8 tiles), read by the epilogue as broadcast
-//    16-byte loads; only the first query tile (the window diagonal) is masked
+//    atomics; only the first query tile (the window diagonal) is masked
 //    i >= j + w; queries past S get lse = +inf (weight 0).
 //
 // CTA layout (320 threads, 2 CTAs per SM): warps 0-7 epilogue (warp w reads
@@ -62,16 +60,39 @@ constexpr int TILE_BYTES = 128 * HD * 2;         // 32 KB: two 128-row x 128-byt
 constexpr int HALF_BYTES = TILE_BYTES / 2;
 constexpr int TMEM_COLS = NACC * BN;             // 256
 
+constexpr int EXT_K = 16;                        // extra MMA K-step of the mass pass
+constexpr int EXT_BYTES = 128 * EXT_K * 2;       // one [128 x 16] 16-bit operand (4 KB)
+
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + TILE_BYTES;
 constexpr int OFF_BAR = OFF_B + NSTAGE * TILE_BYTES;
 constexpr int OFF_MISC = OFF_BAR + 256;
-// A ring of NRK per-tile vectors staged by the producer warp for the epilogue: -lse_i*log2(e)
-// of a query tile (mass pass) or the static ranks of a key tile (sparse LSE pass).
+constexpr int OFF_AEXT = OFF_MISC + 256;         // key-side extension: [1, 1, 1, 0, ...] per row
+constexpr int OFF_BEXT = OFF_AEXT + EXT_BYTES;   // query-side extension per stage: -lse/scale split
+constexpr int OFF_RED = OFF_BEXT + NSTAGE * EXT_BYTES;
+// Sparse LSE pass: ranks of the last NRK key tiles (the extension operands are unused there).
 constexpr int NRK = 8;
-constexpr int OFF_RANK = OFF_MISC + 256;
-constexpr int OFF_RED = OFF_RANK + NRK * BN * 4;
+constexpr int OFF_RANK = OFF_AEXT;
+static_assert(NRK * BN * 4 <= OFF_RED - OFF_AEXT, "rank ring must fit in the extension area");
 constexpr int SMEM_BYTES = OFF_RED + 2 * BM * 4 + 1024;   // + alignment slack
+
+// Byte offset of element (r, k) of a [128 x 16] K-major operand in 8 x 16-byte core matrices
+// (core (r/8, k/8) at (r/8)*256 + (k/8)*128): the layout desc_noswz(addr, 128, 256) reads.
+__device__ __forceinline__ int ext_off(int r, int k) {
+  return (r >> 3) * 256 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
+}
+
+// Round to bf16 / f16 (bits) and return the value kept.
+__device__ __forceinline__ uint16_t round16(float x, bool bf16, float& kept) {
+  if (bf16) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    kept = __bfloat162float(h);
+    return *reinterpret_cast<const uint16_t*>(&h);
+  }
+  const __half h = __float2half_rn(x);
+  kept = __half2float(h);
+  return *reinterpret_cast<const uint16_t*>(&h);
+}
 
 struct TcParams {
   int S, Hq, Hkv, G;
@@ -82,7 +103,7 @@ struct TcParams {
   float* out;            // LSE pass: lse [B*Hq*S]; mass pass: partial sums (workspace)
   int n_groups;          // LSE pass: B*Hq; mass pass: B*Hkv
   int NQT;               // LSE pass: query tiles per head
-  int NT0, TPC, CMAX, NKT, Nf, Np;   // mass pass schedule
+  int NT0, TPC, CMAX, NKT, Nf;   // mass pass schedule
   int per_head;          // mass pass: keep each query head's sum (partials [.., G, 2 halves, 128])
   // sparse LSE pass (MODE 2): static ranks and running cutoffs [B*Hkv*S] of the running top-k
   // mask; key j is kept for query i if j < n_sink, j > i - window, tau_i < 0 or rank_j <= tau_i
@@ -111,8 +132,6 @@ __device__ __forceinline__ Item decode_item(int I, const TcParams& p) {
     it.per_head = 0;
     it.n_tiles = it.tile + 1;
   } else {
-    // Heaviest first: the full-length items of every group (chunk by chunk), then the shorter
-    // tail items; consecutive CTAs take different groups.
     const long long full_total = (long long)p.Nf * p.n_groups;
     if (I < full_total) {
       int local = I / p.n_groups;
@@ -194,6 +213,8 @@ __global__ void __launch_bounds__(THREADS, 2)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
   float* red = reinterpret_cast<float*>(smem + OFF_RED);
+  const uint32_t sAext = s_base + OFF_AEXT;
+  const uint32_t sBext = s_base + OFF_BEXT;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Item it = decode_item<MODE>(blockIdx.x, p);
@@ -208,7 +229,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       ptx::mbar_init(bar_acce + 8 * a, EPI_WARPS);
     }
     ptx::mbar_init(bar_a, 1);
-    if (MODE != 0)
+    if (MODE == 2)
       for (int b = 0; b < NRK; ++b) ptx::mbar_init(bar_rk + 8 * b, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -220,6 +241,20 @@ __global__ void __launch_bounds__(THREADS, 2)
   if (warp == PRODUCER_WARP && lane == 0) {
     ptx::prefetch_tmap(&tmQ);
     ptx::prefetch_tmap(&tmK);
+  }
+  if (MODE == 1 && threadIdx.x < EPI_WARPS * 32) {
+    // The extra K-step adds -lse_i/scale (B side, three 16-bit parts) times 1 (A side) to every
+    // logit, so the accumulator already holds the LSE-offset logit.
+    const uint16_t one = bf16 ? 0x3F80u : 0x3C00u;
+    for (int e = threadIdx.x; e < 128 * EXT_K; e += EPI_WARPS * 32) {
+      const int r = e / EXT_K, k = e % EXT_K;
+      *reinterpret_cast<uint16_t*>(smem + OFF_AEXT + ext_off(r, k)) = k < 3 ? one : 0u;
+    }
+    for (int e = threadIdx.x; e < NSTAGE * 128 * EXT_K; e += EPI_WARPS * 32) {
+      const int st = e / (128 * EXT_K), rem = e % (128 * EXT_K);
+      *reinterpret_cast<uint16_t*>(smem + OFF_BEXT + st * EXT_BYTES + ext_off(rem / EXT_K, rem % EXT_K)) = 0u;
+    }
+    ptx::fence_proxy_async_smem();
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -259,24 +294,34 @@ __global__ void __launch_bounds__(THREADS, 2)
       ptx::tma_load_3d(sA, tmA, bar_a, 0, a_row, a_z);
       ptx::tma_load_3d(sA + HALF_BYTES, tmA, bar_a, 64, a_row, a_z);
     }
+    // Mass pass: the LSE of a tile's 128 queries (4 per lane) is loaded one tile ahead.
+    auto load_lv = [&](int t, float (&lv)[4]) {
+      const int gh = t / it.per_head, u = t % it.per_head;
+      const int i0 = j0 + p.window + BN * (it.chunk * p.TPC + u) + 4 * lane;
+      const float* lrow = p.lse + (size_t)(b_of_group * p.Hq + hkv * p.G + gh) * p.S;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) lv[j] = i0 + j < p.S ? __ldg(lrow + i0 + j) : INFINITY;
+    };
+    float lv[4] = {0.f, 0.f, 0.f, 0.f};
+    if (MODE == 1 && it.n_tiles > 0) load_lv(0, lv);
     int t = 0;
     for (; t < it.n_tiles; ++t) {
       const int s = t % NSTAGE, use = t / NSTAGE;
-      float lv[4];
-      if (MODE == 1) {   // LSE of this tile's 128 queries, 4 per lane, loaded before the wait
-        const int gh = t / it.per_head, u = t % it.per_head;
-        const int i0 = j0 + p.window + BN * (it.chunk * p.TPC + u) + 4 * lane;
-        const float* lrow = p.lse + (size_t)(b_of_group * p.Hq + hkv * p.G + gh) * p.S;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) lv[j] = i0 + j < p.S ? __ldg(lrow + i0 + j) : INFINITY;
-      }
       bool ok = true;
       if (use > 0) ok = ptx::mbar_wait(bar_empty + 8 * s, (use - 1) & 1, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, ok)) break;
+      if (lane == 0) {
+        int row, z;
+        b_coords(t, row, z);
+        const uint32_t dst = sB + s * TILE_BYTES;
+        // Mass pass: the stage also needs this warp's extension rows, so the copy is issued
+        // first (transaction count only) and the arrival comes after they are written.
+        if (MODE == 1) ptx::mbar_expect_tx(bar_full + 8 * s, TILE_BYTES);
+        else ptx::mbar_arrive_expect_tx(bar_full + 8 * s, TILE_BYTES);
+        ptx::tma_load_3d(dst, tmB, bar_full + 8 * s, 0, row, z);
+        ptx::tma_load_3d(dst + HALF_BYTES, tmB, bar_full + 8 * s, 64, row, z);
+      }
       if (MODE == 2) {
-        // Ranks of key tile t for the epilogue's mask.  Buffer t % NRK was last read for tile
-        // t - NRK; the wait above (MMA of tile t - 2 done, which itself waited for the
-        // epilogue to take tile t - 4 out of TMEM) keeps the epilogue past that tile.
         const int kb = t * BN + 4 * lane;
         const int32_t* src = p.ranks + (size_t)kv_z * p.S + kb;
         int4 r4;
@@ -293,24 +338,28 @@ __global__ void __launch_bounds__(THREADS, 2)
         if (lane == 0) ptx::mbar_arrive(bar_rk + 8 * (t % NRK));
       }
       if (MODE == 1) {
-        // -lse*log2(e) of tile t's 128 queries for the epilogue (+inf lse past S -> -inf, weight
-        // 0).  Buffer t % NRK is free by the same pipeline-depth argument as the sparse ranks.
-        float4 n4;
-        n4.x = -lv[0] * KVP_LOG2E;
-        n4.y = -lv[1] * KVP_LOG2E;
-        n4.z = -lv[2] * KVP_LOG2E;
-        n4.w = -lv[3] * KVP_LOG2E;
-        *reinterpret_cast<float4*>(rbuf + (t % NRK) * BN + 4 * lane) = n4;
+        uint8_t* ext = smem + OFF_BEXT + s * EXT_BYTES;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = 4 * lane + j;
+          uint16_t h1, h2 = 0, h3 = 0;
+          if (lv[j] == INFINITY) {
+            h1 = bf16 ? 0xFF80u : 0xFC00u;
+          } else {
+            const float h = -lv[j] * p.inv_scale;
+            float k1, k2, k3;
+            h1 = round16(h, bf16, k1);
+            h2 = round16(h - k1, bf16, k2);
+            h3 = round16((h - k1) - k2, bf16, k3);
+          }
+          *reinterpret_cast<uint16_t*>(ext + ext_off(r, 0)) = h1;
+          *reinterpret_cast<uint16_t*>(ext + ext_off(r, 1)) = h2;
+          *reinterpret_cast<uint16_t*>(ext + ext_off(r, 2)) = h3;
+        }
+        ptx::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar_rk + 8 * (t % NRK));
-      }
-      if (lane == 0) {
-        int row, z;
-        b_coords(t, row, z);
-        const uint32_t dst = sB + s * TILE_BYTES;
-        ptx::mbar_arrive_expect_tx(bar_full + 8 * s, TILE_BYTES);
-        ptx::tma_load_3d(dst, tmB, bar_full + 8 * s, 0, row, z);
-        ptx::tma_load_3d(dst + HALF_BYTES, tmB, bar_full + 8 * s, 64, row, z);
+        if (lane == 0) ptx::mbar_arrive(bar_full + 8 * s);
+        if (t + 1 < it.n_tiles) load_lv(t + 1, lv);
       }
     }
     if (lane == 0) {
@@ -337,6 +386,9 @@ __global__ void __launch_bounds__(THREADS, 2)
             const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
             ptx::mma_f16_ss(d, ptx::desc_sw128(sA + off), ptx::desc_sw128(bs + off), idesc, kk > 0);
           }
+          if (MODE == 1)
+            ptx::mma_f16_ss(d, ptx::desc_noswz(sAext, 128, 256), ptx::desc_noswz(sBext + s * EXT_BYTES, 128, 256),
+                            idesc, 1);
           ptx::mma_commit(bar_empty + 8 * s);
           ptx::mma_commit(bar_accf + 8 * a);
         }
@@ -443,8 +495,7 @@ __global__ void __launch_bounds__(THREADS, 2)
         unpack2(s23, q2, q3);
         l += (q0 + q1) + (q2 + q3);
       } else {
-        // the accumulator holds q.k; the producer staged -lse_i*log2(e) of the tile's queries
-        // (-inf past S: weight 0) in shared memory
+        // the accumulator holds (q.k - lse_i/scale); past S it is -inf
         const int u = t % it.per_head;
         const bool diag = (it.chunk == 0 && u == 0);
         if (diag) {
@@ -452,18 +503,12 @@ __global__ void __launch_bounds__(THREADS, 2)
           for (int c = 0; c < 64; ++c)
             if (half * 64 + c < r) v[c] = __float_as_uint(-INFINITY);
         }
-        if (!ptx::mbar_wait(bar_rk + 8 * (t % NRK), (t / NRK) & 1, abort_flag, p.status)) {
-          ok = false;
-          break;
-        }
-        const float4* nl = reinterpret_cast<const float4*>(rbuf + (t % NRK) * BN + half * 64);
+        const uint64_t zero2 = 0;
 #pragma unroll
         for (int c = 0; c < 64; c += 4) {
-          const float4 n = nl[c >> 2];
           float x0, x1, x2, x3;
-          unpack2(ffma2(pack2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), c2x2, pack2(n.x, n.y)), x0, x1);
-          unpack2(ffma2(pack2(__uint_as_float(v[c + 2]), __uint_as_float(v[c + 3])), c2x2, pack2(n.z, n.w)),
-                  x2, x3);
+          unpack2(ffma2(pack2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), c2x2, zero2), x0, x1);
+          unpack2(ffma2(pack2(__uint_as_float(v[c + 2]), __uint_as_float(v[c + 3])), c2x2, zero2), x2, x3);
           acc01 = fadd2(acc01, pack2(fast_exp2(x0), fast_exp2(x1)));
           acc23 = fadd2(acc23, pack2(fast_exp2(x2), fast_exp2(x3)));
         }
@@ -685,7 +730,6 @@ cudaError_t launch_fam_tc(const void* q, const void* k, const float* lse, int dt
   p.CMAX = f.CMAX;
   p.NKT = f.NKT;
   p.Nf = f.Nf;
-  p.Np = f.Np;
   p.per_head = per_head;
   p.status = status;
   const long long items = (long long)(f.Nf + f.Np) * p.n_groups;
