@@ -45,8 +45,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel source is unchanged (sha256 of the .cu file at capture time).
 NCU_TRAFFIC = {
     # ncu --set full of attn_tc_kernel<1> on the benchmark layer (S = 8192; the kernel source hashed
-    # below): 115.28 MB read + 3.61 MB written per launch (profiles/attn_tc_fam_qwen3-4b-layer_S8192.md)
-    "future_attn_mass": {"sha": "a7e88300ec2fd2a9", "bytes": 115278848 + 3609088},
+    # below): 115.90 MB read + 3.17 MB written per launch (profiles/attn_tc_fam_qwen3-4b-layer_S8192.md)
+    "future_attn_mass": {"sha": "e4f27acd651e111d", "bytes": 115897856 + 3173376},
 }
 
 
