@@ -197,7 +197,7 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 2)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const TcParams p, const bool bf16) {
+                   const __grid_constant__ CUtensorMap tmE, const TcParams p, const bool bf16) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = ptx::smem_u32(smem);
@@ -250,9 +250,11 @@ __global__ void __launch_bounds__(THREADS, 2)
       const int r = e / EXT_K, k = e % EXT_K;
       *reinterpret_cast<uint16_t*>(smem + OFF_AEXT + ext_off(r, k)) = k < 3 ? one : 0u;
     }
-    for (int e = threadIdx.x; e < NSTAGE * 128 * EXT_K; e += EPI_WARPS * 32) {
-      const int st = e / (128 * EXT_K), rem = e % (128 * EXT_K);
-      *reinterpret_cast<uint16_t*>(smem + OFF_BEXT + st * EXT_BYTES + ext_off(rem / EXT_K, rem % EXT_K)) = 0u;
+    // B side, per stage: rows 0..127 of k = 0..7 (written by TMA from the prepared array) at
+    // 16-byte row pitch, then the k = 8..15 half, which stays zero.
+    for (int e = threadIdx.x; e < NSTAGE * EXT_BYTES / 16; e += EPI_WARPS * 32) {
+      const int st = e / (EXT_BYTES / 16), off = (e % (EXT_BYTES / 16)) * 16;
+      if (off >= EXT_BYTES / 2) *reinterpret_cast<uint4*>(smem + OFF_BEXT + st * EXT_BYTES + off) = make_uint4(0u, 0u, 0u, 0u);
     }
     ptx::fence_proxy_async_smem();
   }
@@ -294,16 +296,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       ptx::tma_load_3d(sA, tmA, bar_a, 0, a_row, a_z);
       ptx::tma_load_3d(sA + HALF_BYTES, tmA, bar_a, 64, a_row, a_z);
     }
-    // Mass pass: the LSE of a tile's 128 queries (4 per lane) is loaded one tile ahead.
-    auto load_lv = [&](int t, float (&lv)[4]) {
-      const int gh = t / it.per_head, u = t % it.per_head;
-      const int i0 = j0 + p.window + BN * (it.chunk * p.TPC + u) + 4 * lane;
-      const float* lrow = p.lse + (size_t)(b_of_group * p.Hq + hkv * p.G + gh) * p.S;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) lv[j] = i0 + j < p.S ? __ldg(lrow + i0 + j) : INFINITY;
-    };
-    float lv[4] = {0.f, 0.f, 0.f, 0.f};
-    if (MODE == 1 && it.n_tiles > 0) load_lv(0, lv);
+    if (lane == 0) ptx::prefetch_tmap(&tmE);
     int t = 0;
     for (; t < it.n_tiles; ++t) {
       const int s = t % NSTAGE, use = t / NSTAGE;
@@ -314,12 +307,12 @@ __global__ void __launch_bounds__(THREADS, 2)
         int row, z;
         b_coords(t, row, z);
         const uint32_t dst = sB + s * TILE_BYTES;
-        // Mass pass: the stage also needs this warp's extension rows, so the copy is issued
-        // first (transaction count only) and the arrival comes after they are written.
-        if (MODE == 1) ptx::mbar_expect_tx(bar_full + 8 * s, TILE_BYTES);
-        else ptx::mbar_arrive_expect_tx(bar_full + 8 * s, TILE_BYTES);
+        // Mass pass: the stage also receives the 128 query rows' -lse/scale extension (three
+        // 16-bit parts per row, prepared in global memory) by its own TMA box.
+        ptx::mbar_arrive_expect_tx(bar_full + 8 * s, TILE_BYTES + (MODE == 1 ? EXT_BYTES / 2 : 0));
         ptx::tma_load_3d(dst, tmB, bar_full + 8 * s, 0, row, z);
         ptx::tma_load_3d(dst + HALF_BYTES, tmB, bar_full + 8 * s, 64, row, z);
+        if (MODE == 1) ptx::tma_load_3d(sBext + s * EXT_BYTES, &tmE, bar_full + 8 * s, 0, row, z);
       }
       if (MODE == 2) {
         const int kb = t * BN + 4 * lane;
@@ -336,30 +329,6 @@ __global__ void __launch_bounds__(THREADS, 2)
         *reinterpret_cast<int4*>(rbuf + (t % NRK) * BN + 4 * lane) = r4;
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bar_rk + 8 * (t % NRK));
-      }
-      if (MODE == 1) {
-        uint8_t* ext = smem + OFF_BEXT + s * EXT_BYTES;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int r = 4 * lane + j;
-          uint16_t h1, h2 = 0, h3 = 0;
-          if (lv[j] == INFINITY) {
-            h1 = bf16 ? 0xFF80u : 0xFC00u;
-          } else {
-            const float h = -lv[j] * p.inv_scale;
-            float k1, k2, k3;
-            h1 = round16(h, bf16, k1);
-            h2 = round16(h - k1, bf16, k2);
-            h3 = round16((h - k1) - k2, bf16, k3);
-          }
-          *reinterpret_cast<uint16_t*>(ext + ext_off(r, 0)) = h1;
-          *reinterpret_cast<uint16_t*>(ext + ext_off(r, 1)) = h2;
-          *reinterpret_cast<uint16_t*>(ext + ext_off(r, 2)) = h3;
-        }
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar_full + 8 * s);
-        if (t + 1 < it.n_tiles) load_lv(t + 1, lv);
       }
     }
     if (lane == 0) {
@@ -387,7 +356,7 @@ __global__ void __launch_bounds__(THREADS, 2)
             ptx::mma_f16_ss(d, ptx::desc_sw128(sA + off), ptx::desc_sw128(bs + off), idesc, kk > 0);
           }
           if (MODE == 1)
-            ptx::mma_f16_ss(d, ptx::desc_noswz(sAext, 128, 256), ptx::desc_noswz(sBext + s * EXT_BYTES, 128, 256),
+            ptx::mma_f16_ss(d, ptx::desc_noswz(sAext, 128, 256), ptx::desc_noswz(sBext + s * EXT_BYTES, 2048, 128),
                             idesc, 1);
           ptx::mma_commit(bar_empty + 8 * s);
           ptx::mma_commit(bar_accf + 8 * a);
@@ -564,6 +533,29 @@ __global__ void __launch_bounds__(THREADS, 2)
 }
 
 // F[group, j] = sum over the chunks of key tile j/128 of the partial sums, in chunk order.
+// Query-side extension of the mass pass: row i of head z holds -lse[z, i]/scale split into three
+// 16-bit parts (exactly representable sum to ~2^-24 relative), then zeros; rows i >= S (the
+// padding the last query tiles read) hold -inf, so those queries get weight exactly 0.
+__global__ void ext_prep_kernel(const float* __restrict__ lse, int BHq, int S, int S_pad,
+                                float inv_scale, bool bf16, uint4* __restrict__ ext) {
+  const long long total = (long long)BHq * S_pad;
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (long long)gridDim.x * blockDim.x) {
+    const int z = (int)(e / S_pad), i = (int)(e % S_pad);
+    uint16_t h1, h2 = 0, h3 = 0;
+    if (i >= S) {
+      h1 = bf16 ? 0xFF80u : 0xFC00u;
+    } else {
+      const float h = -lse[(size_t)z * S + i] * inv_scale;
+      float k1, k2, k3;
+      h1 = round16(h, bf16, k1);
+      h2 = round16(h - k1, bf16, k2);
+      h3 = round16((h - k1) - k2, bf16, k3);
+    }
+    ext[e] = make_uint4((uint32_t)h1 | ((uint32_t)h2 << 16), (uint32_t)h3, 0u, 0u);
+  }
+}
+
 __global__ void __launch_bounds__(BM) fam_reduce_kernel(const float* __restrict__ part, int S, int NT0,
                                                         int TPC, int CMAX, int NKT,
                                                         float* __restrict__ F) {
@@ -632,6 +624,22 @@ bool make_tmap(CUtensorMap* m, const void* base, int dtype, int n_heads, int S) 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor map of the mass pass's query-side extension [n_heads, S_pad, 8] (16-byte rows, boxes of
+// 128 rows, no swizzle: a box lands as 128 contiguous 16-byte rows).
+bool make_ext_tmap(CUtensorMap* m, const void* base, int dtype, int n_heads, int S_pad) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {8, (cuuint64_t)S_pad, (cuuint64_t)n_heads};
+  cuuint64_t strides[2] = {16, (cuuint64_t)S_pad * 16};
+  cuuint32_t box[3] = {8, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt =
+      dtype == KVP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct FamSched {
   int NT0, TPC, CMAX, NKT, Nf, Np;
 };
@@ -660,13 +668,13 @@ FamSched fam_schedule(AttnShape s, int window) {
 }
 
 template <int MODE>
-cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const TcParams& p, int grid,
-                      bool bf16, cudaStream_t st) {
+cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& te, const TcParams& p,
+                      int grid, bool bf16, cudaStream_t st) {
   auto kern = attn_tc_kernel<MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   count_launches(1);
-  kern<<<grid, THREADS, SMEM_BYTES, st>>>(tq, tk, p, bf16);
+  kern<<<grid, THREADS, SMEM_BYTES, st>>>(tq, tk, te, p, bf16);
   return cudaGetLastError();
 }
 
@@ -676,10 +684,16 @@ bool tc_supported(int dtype, AttnShape s) {
   return (dtype == KVP_BF16 || dtype == KVP_F16) && s.head_dim == HD && encode_fn() != nullptr;
 }
 
+// Workspace of the mass pass: partial sums, then the query-side extension (16 bytes per query
+// row, S + 128 rows per query head).
+size_t fam_partial_bytes(AttnShape s, const FamSched& f, int per_head) {
+  const size_t heads = per_head ? (size_t)2 * (s.h_q / s.h_kv) : 1;
+  return (((size_t)s.n_batch * s.h_kv * f.NKT * f.CMAX * heads * BM * sizeof(float)) + 255) & ~(size_t)255;
+}
+
 size_t fam_tc_workspace_size(AttnShape s, int window, int per_head) {
   const FamSched f = fam_schedule(s, window);
-  const size_t heads = per_head ? (size_t)2 * (s.h_q / s.h_kv) : 1;
-  return (size_t)s.n_batch * s.h_kv * f.NKT * f.CMAX * heads * BM * sizeof(float);
+  return fam_partial_bytes(s, f, per_head) + (size_t)s.n_batch * s.h_q * (s.seq_len + BN) * 16;
 }
 
 cudaError_t launch_lse_tc(const void* q, const void* k, int dtype, AttnShape s, float scale,
@@ -704,9 +718,9 @@ cudaError_t launch_lse_tc(const void* q, const void* k, int dtype, AttnShape s, 
     p.n_sink = mask->n_sink;
     p.window = mask->window;
     p.ranks_vec = s.seq_len % 4 == 0 && ((uintptr_t)mask->ranks & 15) == 0;
-    return launch_tc<2>(tq, tk, p, p.n_groups * p.NQT, dtype == KVP_BF16, st);
+    return launch_tc<2>(tq, tk, tk, p, p.n_groups * p.NQT, dtype == KVP_BF16, st);
   }
-  return launch_tc<0>(tq, tk, p, p.n_groups * p.NQT, dtype == KVP_BF16, st);
+  return launch_tc<0>(tq, tk, tk, p, p.n_groups * p.NQT, dtype == KVP_BF16, st);
 }
 
 cudaError_t launch_fam_tc(const void* q, const void* k, const float* lse, int dtype, AttnShape s,
@@ -734,12 +748,26 @@ cudaError_t launch_fam_tc(const void* q, const void* k, const float* lse, int dt
   p.status = status;
   const long long items = (long long)(f.Nf + f.Np) * p.n_groups;
   if (items > 0) {
-    CUtensorMap tq, tk;
-    if (!make_tmap(&tq, q, dtype, s.n_batch * s.h_q, s.seq_len) ||
-        !make_tmap(&tk, k, dtype, s.n_batch * s.h_kv, s.seq_len))
+    const int BHq = s.n_batch * s.h_q, S_pad = s.seq_len + BN;
+    void* ext = (char*)ws + fam_partial_bytes(s, f, per_head);
+    CUtensorMap tq, tk, te;
+    if (!make_tmap(&tq, q, dtype, BHq, s.seq_len) ||
+        !make_tmap(&tk, k, dtype, s.n_batch * s.h_kv, s.seq_len) ||
+        !make_ext_tmap(&te, ext, dtype, BHq, S_pad))
       return cudaErrorInvalidValue;
     if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
-    cudaError_t e = launch_tc<1>(tq, tk, p, (int)items, dtype == KVP_BF16, st);
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long rows = (long long)BHq * S_pad;
+    long long blocks = (rows + 255) / 256;
+    if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
+    count_launches(1);
+    ext_prep_kernel<<<(unsigned)blocks, 256, 0, st>>>(lse, BHq, s.seq_len, S_pad, p.inv_scale,
+                                                     dtype == KVP_BF16, (uint4*)ext);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = launch_tc<1>(tq, tk, te, p, (int)items, dtype == KVP_BF16, st);
     if (e != cudaSuccess) return e;
   }
   count_launches(1);
