@@ -44,9 +44,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic of one launch of the dominant kernel from an ncu capture, valid only while the
 # kernel source is unchanged (sha256 of the .cu file at capture time).
 NCU_TRAFFIC = {
-    # ncu --set full of attn_tc_kernel<1> on the benchmark layer (S = 8192; the kernel source hashed
-    # below): 115.90 MB read + 3.17 MB written per launch (profiles/attn_tc_fam_qwen3-4b-layer_S8192.md)
-    "future_attn_mass": {"sha": "e4f27acd651e111d", "bytes": 115897856 + 3173376},
+    # ncu --set full of attn_tc_kernel<1> / <0> on the benchmark layer (S = 8192; the kernel source
+    # hashed below), DRAM bytes read + written per launch (profiles/attn_tc_fam_qwen3-4b-layer_S8192.md,
+    # profiles/attn_tc_lse_qwen3-4b-layer_S8192.md)
+    "future_attn_mass": {"sha": "6b3bb9168e8a7b20", "bytes": 135898368 + 3416064},
+    "lse_pass": {"sha": "6b3bb9168e8a7b20", "bytes": 83911936 + 2372096},
 }
 
 
