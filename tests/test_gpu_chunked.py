@@ -79,3 +79,14 @@ def test_chunk_compress_rejects_small_output(kvp):
            "score": torch.empty(R, 8, device="cuda"), "pos": torch.empty(R, 8, dtype=torch.int32, device="cuda")}
     with pytest.raises(kvp.KvpError):
         kvp.kvp_chunk_compress(None, 0, ck, ck, cs, 0, 32, 4, 8, out)
+
+
+def test_chunked_budget_below_sinks_plus_window(kvp):
+    """budget < n_sink + n_recent: every step keeps n_sink + n_recent entries (the effective budget)."""
+    R, D, S, C, b, ns, nr = 3, 64, 700, 100, 10, 4, 32
+    gen = torch.Generator().manual_seed(5)
+    k = torch.randn(R, S, D, generator=gen).to(torch.float16)
+    v = torch.randn(R, S, D, generator=gen).to(torch.float16)
+    s = kvp_inputs.make_scores(R, S, seed=11)
+    cache, n = _run_loop(kvp, k, v, s, C, b, ns, nr)
+    assert n == ns + nr

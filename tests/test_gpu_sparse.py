@@ -103,3 +103,32 @@ def test_sparse_lse_qwen3_4b_layer_full_size(kvp):
                                  ranks[h:h + 1].cpu().numpy(), want_tau[None], w.head_dim ** -0.5,
                                  w.n_sink, w.window, rows=rows)
     check_lse(np64(lse[0, h * G:(h + 1) * G])[:, rows], want, "full-size sparse LSE")
+
+
+@pytest.mark.parametrize("S", [1, 77, 129])
+def test_sparse_lse_short_sequences(kvp, S):
+    """A single (partial) tile, S below the window, and one full tile plus one key."""
+    q, kk, ranks, tau, lse = _sparse_case(kvp, "bf16", 128, S, 4, 2, 2, 16, 5, seed=S)
+    want = oracle.sparse_row_lse(q[0], kk[0], ranks.numpy(), tau, 128 ** -0.5, 2, 16)
+    check_lse(np64(lse[0]), want, f"S{S}")
+
+
+def test_sparse_lse_qwen3_8b_131k_sampled(kvp):
+    """131072 tokens, one KV head: cutoffs in full, the sparse LSE on 96 sampled rows."""
+    w = kvp_inputs.QWEN3_8B_131K
+    x = kvp_inputs.make_prefill_layer(w, 0, device="cuda", seq_len=w.seq_len)
+    q = x["q"][None, :w.group].contiguous()          # KV head 0 and its query heads
+    k = x["k"][None, :1].contiguous()
+    k_lr = w.budget - w.n_sink - w.window
+    ranks = kvp_inputs.make_static_ranks(1, w.seq_len, seed=9, device="cuda")
+    tau = kvp.kvp_topk_cutoffs(ranks, w.n_sink, w.window, k_lr)
+    lse = kvp.kvp_sparse_lse_pass(q, k, ranks, tau, w.n_sink, w.window)
+    torch.cuda.synchronize()
+    kvp.kvp_check_device_status()
+    want_tau = oracle.fenwick_cutoffs(ranks[0].cpu().numpy(), w.n_sink, w.window, k_lr)
+    assert (tau[0].cpu().numpy() == want_tau).all()
+    rows = np.unique(np.concatenate([np.random.default_rng(1).integers(0, w.seq_len, 80),
+                                     np.arange(w.seq_len - 16, w.seq_len)]))
+    want = oracle.sparse_row_lse(q[0].cpu(), k[0].cpu(), ranks.cpu().numpy(), want_tau[None],
+                                 w.head_dim ** -0.5, w.n_sink, w.window, rows=rows)
+    check_lse(np64(lse[0])[:, rows], want, "131k sparse LSE")
