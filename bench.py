@@ -491,13 +491,16 @@ def target_measure(kvp, x, plan, w, K, W, flush, peak, stream, dev):
 
 def sparse_lse_measure(kvp, x, w, K, W, flush, peak, stream, dev):
     """KVpop's running top-k sparse attention on the same layer: the cutoffs from seeded static
-    ranks (long-range budget k = budget - sinks - window), then the sparse row LSE.  The pass
-    scores every causal pair and masks per element, so its TFLOP/s counts the causal pairs."""
+    ranks (long-range budget k = budget - sinks - window), then the sparse row LSE (rank-ordered
+    key stream where it is shorter).  Its TFLOP/s counts the causal pairs, so skipped tiles show
+    up as a rate above the dense pass's."""
     S, D = w.seq_len, w.head_dim
     k_lr = w.budget - w.n_sink - w.window
     ranks = kvp_inputs.make_static_ranks(w.h_kv, S, seed=3, device=dev)
     tau = torch.empty_like(ranks)
     lse = torch.empty(1, w.h_q, S, device=dev)
+    sws = torch.empty(max(1, kvp.kvp_sparse_lse_workspace_size(x["q"].dtype, 1, w.h_q, w.h_kv, S, D)),
+                      dtype=torch.uint8, device=dev)
 
     def run(ev=None):
         if ev:
@@ -505,7 +508,7 @@ def sparse_lse_measure(kvp, x, w, K, W, flush, peak, stream, dev):
         kvp.kvp_topk_cutoffs(ranks, w.n_sink, w.window, k_lr, tau=tau)
         if ev:
             ev[1].record(stream)
-        kvp.kvp_sparse_lse_pass(x["q"], x["k"], ranks, tau, w.n_sink, w.window, lse=lse)
+        kvp.kvp_sparse_lse_pass(x["q"], x["k"], ranks, tau, w.n_sink, w.window, lse=lse, workspace=sws)
         if ev:
             ev[2].record(stream)
 

@@ -176,11 +176,20 @@ int kvp_topk_cutoffs(const int32_t* ranks, int n_heads, int seq_len, int n_sink,
  * tau[i] < 0 (fewer than k eligible tokens) keeps every eligible token.
  * q, k, lse as in kvp_lse_pass; ranks and tau [n_batch, h_kv, seq_len] int32
  * (kvp_topk_cutoffs' input and output; any int32 values are accepted, the
- * mask is applied as written).
+ * mask is applied as written).  workspace: kvp_sparse_lse_workspace_size()
+ * bytes, 256-byte aligned (0 for the fp32 path).  On the tensor-core path a
+ * query tile whose first row has a cutoff streams, instead of every causal
+ * key tile, the tiles holding its sinks and windows plus the keys in rank
+ * order up to that cutoff (the workspace holds the inverse permutation and
+ * the keys in rank order), whenever that is fewer tiles; ranks that are not a
+ * permutation fall back to the dense stream.
  * ------------------------------------------------------------------------- */
+size_t kvp_sparse_lse_workspace_size(int dtype, int n_batch, int h_q, int h_kv, int seq_len,
+                                     int head_dim);
 int kvp_sparse_lse_pass(const void* q, const void* k, const int32_t* ranks, const int32_t* tau,
                         int dtype, int n_batch, int h_q, int h_kv, int seq_len, int head_dim,
-                        float sm_scale, int n_sink, int window, float* lse, kvp_stream_t stream);
+                        float sm_scale, int n_sink, int window, float* lse, void* workspace,
+                        size_t workspace_bytes, kvp_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Ranks of score rows (static ranks; the optimal ranking of the eviction cost).

@@ -32,7 +32,8 @@ SIGNATURES = {
     "kvp_future_attn_target": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _F, _I, _P, _P, _P, _P,
                                     _SZ, _P]),
     "kvp_topk_cutoffs": (_I, [_P, _I, _I, _I, _I, _I, _P, _P]),
-    "kvp_sparse_lse_pass": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P]),
+    "kvp_sparse_lse_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "kvp_sparse_lse_pass": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _SZ, _P]),
     "kvp_soft_topk_budgets": (_I, [_P, _I, _D, _I, _P, _P, _P]),
     "kvp_select_topk": (_I, [_P, _I, _I, _I64, _P, _I, _I, _P, _I, _P, _P]),
     "kvp_compact_kv": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P]),
@@ -158,7 +159,13 @@ def kvp_topk_cutoffs(ranks, n_sink, window, k, tau=None, stream=None):
     return tau
 
 
-def kvp_sparse_lse_pass(q, k, ranks, tau, n_sink, window, sm_scale=None, lse=None, stream=None):
+def kvp_sparse_lse_workspace_size(dtype, n_batch, h_q, h_kv, seq_len, head_dim):
+    dt = _DTYPE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return int(load().kvp_sparse_lse_workspace_size(dt, n_batch, h_q, h_kv, seq_len, head_dim))
+
+
+def kvp_sparse_lse_pass(q, k, ranks, tau, n_sink, window, sm_scale=None, lse=None, workspace=None,
+                        stream=None):
     """Sparse row LSE under the running top-k mask: q [B,H_q,S,D], k [B,H_kv,S,D], ranks and
     tau int32 [B,H_kv,S] -> lse fp32 [B,H_q,S]."""
     squeeze = q.dim() == 3
@@ -178,9 +185,13 @@ def kvp_sparse_lse_pass(q, k, ranks, tau, n_sink, window, sm_scale=None, lse=Non
     _need(lse, "lse", torch.float32)
     if lse.numel() != B * Hq * S:
         raise ValueError("lse has the wrong size")
+    need = kvp_sparse_lse_workspace_size(_dtype(q4), B, Hq, Hkv, S, D)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = load().kvp_sparse_lse_pass(_ptr(q4), _ptr(k4), _ptr(ranks), _ptr(tau), _dtype(q4), B, Hq, Hkv,
                                     S, D, float(sm_scale), int(n_sink), int(window), _ptr(lse),
-                                    _stream(stream))
+                                    _ptr(workspace), ws_bytes, _stream(stream))
     _check("kvp_sparse_lse_pass", rc)
     return lse[0] if squeeze and lse.dim() == 3 else lse
 

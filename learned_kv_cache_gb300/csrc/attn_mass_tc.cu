@@ -111,6 +111,11 @@ struct TcParams {
   const int32_t* tau;
   int n_sink;
   int ranks_vec;         // ranks rows are 16-byte aligned (S % 4 == 0): int4 loads
+  // Rank-ordered stream of the sparse pass (null: dense streaming only): inv[B*Hkv*S] holds the
+  // position of each rank (the inverse permutation) and the third tensor map the keys in rank
+  // order; *perm_ok is zero when the ranks were not a permutation (then every tile is dense).
+  const int32_t* inv;
+  const int* perm_ok;
   int* status;
 };
 
@@ -217,7 +222,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   const uint32_t sBext = s_base + OFF_BEXT;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const Item it = decode_item<MODE>(blockIdx.x, p);
+  Item it = decode_item<MODE>(blockIdx.x, p);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
@@ -241,6 +246,19 @@ __global__ void __launch_bounds__(THREADS, 2)
   if (warp == PRODUCER_WARP && lane == 0) {
     ptx::prefetch_tmap(&tmQ);
     ptx::prefetch_tmap(&tmK);
+  }
+  int* tau_red = reinterpret_cast<int*>(smem + OFF_MISC + 16);      // sparse pass: [4] max, [4] min
+  if (MODE == 2 && p.inv != nullptr && warp < 4) {
+    // cutoff range over the query tile's rows (rows past S ignored)
+    const int kvz = (it.group / p.Hq) * p.Hkv + (it.group % p.Hq) / p.G;
+    const int i = it.tile * BM + threadIdx.x;
+    const int tv = i < p.S ? __ldg(p.tau + (size_t)kvz * p.S + i) : -1;
+    const int vmax = __reduce_max_sync(0xffffffffu, i < p.S ? tv : INT_MIN);
+    const int vmin = __reduce_min_sync(0xffffffffu, i < p.S ? tv : INT_MAX);
+    if (lane == 0) {
+      tau_red[warp] = vmax;
+      tau_red[4 + warp] = vmin;
+    }
   }
   if (MODE == 1 && threadIdx.x < EPI_WARPS * 32) {
     // The extra K-step adds -lse_i/scale (B side, three 16-bit parts) times 1 (A side) to every
@@ -276,10 +294,42 @@ __global__ void __launch_bounds__(THREADS, 2)
     b_of_group = it.group / p.Hkv;
     hkv = it.group % p.Hkv;
   }
+  // Sparse pass, rank-ordered plan of a query tile whose rows all have a cutoff: the key tiles
+  // holding the sinks and the protected windows in position order (eligible keys there are
+  // dropped), then the keys in rank order up to the largest cutoff of the tile (eligible keys of
+  // rank <= the row's cutoff are kept).  Used when it streams fewer tiles than the dense causal
+  // row.
+  bool rank_mode = false;
+  int st_end = 0, wt0 = 0, n_pos = 0;
+  if (MODE == 2 && p.inv != nullptr && *p.perm_ok) {
+    const int i0 = it.tile * BM;
+    const int tmax = max(max(tau_red[0], tau_red[1]), max(tau_red[2], tau_red[3]));
+    const int tmin = min(min(tau_red[4], tau_red[5]), min(tau_red[6], tau_red[7]));
+    if (tmin >= 0) {       // every row of the tile has a cutoff (the cutoffs need not be monotone)
+      const int wlo = i0 - p.window + 1;
+      wt0 = wlo > 0 ? wlo / BN : 0;
+      const int sink_tiles = (p.n_sink + BN - 1) / BN;
+      st_end = sink_tiles < wt0 ? sink_tiles : wt0;
+      n_pos = st_end + (it.tile - wt0 + 1);
+      const int n_rank = tmax / BN + 1;
+      if (n_pos + n_rank < it.tile + 1) {
+        rank_mode = true;
+        it.n_tiles = n_pos + n_rank;
+      }
+    }
+  }
+  // key tile (position order) of streamed tile t, or -1 for a rank-ordered tile
+  auto key_tile = [&](int t) -> int {
+    if (!rank_mode) return t;
+    if (t < st_end) return t;
+    if (t < n_pos) return wt0 + (t - st_end);
+    return -1;
+  };
   const int j0 = it.tile * BM;     // mass pass: first key of the tile
   auto b_coords = [&](int t, int& row, int& z) {
     if (MODE != 1) {
-      row = t * BN;
+      const int kt = key_tile(t);
+      row = kt >= 0 ? kt * BN : (t - n_pos) * BN;
       z = kv_z;
     } else {
       const int gh = t / it.per_head, u = t % it.per_head;
@@ -310,23 +360,33 @@ __global__ void __launch_bounds__(THREADS, 2)
         // Mass pass: the stage also receives the 128 query rows' -lse/scale extension (three
         // 16-bit parts per row, prepared in global memory) by its own TMA box.
         ptx::mbar_arrive_expect_tx(bar_full + 8 * s, TILE_BYTES + (MODE == 1 ? EXT_BYTES / 2 : 0));
-        ptx::tma_load_3d(dst, tmB, bar_full + 8 * s, 0, row, z);
-        ptx::tma_load_3d(dst + HALF_BYTES, tmB, bar_full + 8 * s, 64, row, z);
+        // sparse pass, rank-ordered tiles: the keys in rank order (third tensor map)
+        const CUtensorMap* src = (MODE == 2 && rank_mode && key_tile(t) < 0) ? &tmE : tmB;
+        ptx::tma_load_3d(dst, src, bar_full + 8 * s, 0, row, z);
+        ptx::tma_load_3d(dst + HALF_BYTES, src, bar_full + 8 * s, 64, row, z);
         if (MODE == 1) ptx::tma_load_3d(sBext + s * EXT_BYTES, &tmE, bar_full + 8 * s, 0, row, z);
       }
       if (MODE == 2) {
-        const int kb = t * BN + 4 * lane;
-        const int32_t* src = p.ranks + (size_t)kv_z * p.S + kb;
-        int4 r4;
-        if (p.ranks_vec && kb + 3 < p.S) {
-          r4 = __ldg(reinterpret_cast<const int4*>(src));
+        // Per-column data of the tile for the epilogue's mask: the ranks of a position-ordered
+        // tile (dense plan), +inf ranks for the sink and window tiles of the rank-ordered plan,
+        // the positions of a rank-ordered tile.
+        const int kt = key_tile(t);
+        if (rank_mode && kt >= 0) {
+          *reinterpret_cast<int4*>(rbuf + (t % NRK) * BN + 4 * lane) = make_int4(INT_MAX, INT_MAX, INT_MAX, INT_MAX);
         } else {
-          r4.x = kb < p.S ? __ldg(src) : INT_MAX;
-          r4.y = kb + 1 < p.S ? __ldg(src + 1) : INT_MAX;
-          r4.z = kb + 2 < p.S ? __ldg(src + 2) : INT_MAX;
-          r4.w = kb + 3 < p.S ? __ldg(src + 3) : INT_MAX;
+          const int kb = (kt >= 0 ? kt : t - n_pos) * BN + 4 * lane;
+          const int32_t* src = (rank_mode ? p.inv : p.ranks) + (size_t)kv_z * p.S + kb;
+          int4 r4;
+          if (p.ranks_vec && kb + 3 < p.S) {
+            r4 = __ldg(reinterpret_cast<const int4*>(src));
+          } else {
+            r4.x = kb < p.S ? __ldg(src) : INT_MAX;
+            r4.y = kb + 1 < p.S ? __ldg(src + 1) : INT_MAX;
+            r4.z = kb + 2 < p.S ? __ldg(src + 2) : INT_MAX;
+            r4.w = kb + 3 < p.S ? __ldg(src + 3) : INT_MAX;
+          }
+          *reinterpret_cast<int4*>(rbuf + (t % NRK) * BN + 4 * lane) = r4;
         }
-        *reinterpret_cast<int4*>(rbuf + (t % NRK) * BN + 4 * lane) = r4;
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bar_rk + 8 * (t % NRK));
       }
@@ -398,16 +458,39 @@ __global__ void __launch_bounds__(THREADS, 2)
       if (lane == 0) ptx::mbar_arrive(bar_acce + 8 * a);
 
       if (MODE != 1) {
-        const bool diag = (t == it.tile);
+        const int kt = key_tile(t);
+        const bool diag = (kt == it.tile);
         if (diag) {
 #pragma unroll
           for (int c = 0; c < 64; ++c)
             if (half * 64 + c > r) v[c] = __float_as_uint(-INFINITY);
         }
-        if (MODE == 2) {
+        if (MODE == 2 && rank_mode && kt < 0) {
+          // rank-ordered tile: column c holds the key of rank rb + c at position pos[c]; kept
+          // when that key is eligible for the row and its rank is within the row's cutoff
+          if (!ptx::mbar_wait(bar_rk + 8 * (t % NRK), (t / NRK) & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          const int* ps = rbuf + (t % NRK) * BN + half * 64;
+          const int cmax = tau_eff - ((t - n_pos) * BN + half * 64);   // rank within the cutoff: c <= cmax
+          const int span = row_i - p.window - p.n_sink;                // eligible: 0 <= pos - n_sink <= span
+#pragma unroll
+          for (int g4 = 0; g4 < 16; ++g4) {
+            const int4 p4 = *reinterpret_cast<const int4*>(ps + 4 * g4);
+            const int c = 4 * g4;
+            const int d0 = p4.x - p.n_sink, d1 = p4.y - p.n_sink, d2 = p4.z - p.n_sink, d3 = p4.w - p.n_sink;
+            if (d0 < 0 || d0 > span || c > cmax) v[c] = 0xff800000u;
+            if (d1 < 0 || d1 > span || c + 1 > cmax) v[c + 1] = 0xff800000u;
+            if (d2 < 0 || d2 > span || c + 2 > cmax) v[c + 2] = 0xff800000u;
+            if (d3 < 0 || d3 > span || c + 3 > cmax) v[c + 3] = 0xff800000u;
+          }
+        } else if (MODE == 2) {
           // Columns cs <= c <= cw are eligible (neither sink nor in the protected window) and
-          // are dropped when their rank is past the row's cutoff.
-          const int jb = t * BN + half * 64;
+          // are dropped when their rank is past the row's cutoff.  (The sink and window tiles of
+          // the rank-ordered plan carry rank +inf: their eligible keys are counted by the
+          // rank-ordered tiles.)
+          const int jb = kt * BN + half * 64;
           const int cw = row_i - p.window - jb, cs = p.n_sink - jb;
           const int lo = cs > 0 ? cs : 0, hi = cw < 63 ? cw : 63;
           if (__any_sync(0xffffffffu, tau_eff != INT_MAX && lo <= hi)) {
@@ -556,6 +639,35 @@ __global__ void ext_prep_kernel(const float* __restrict__ lse, int BHq, int S, i
   }
 }
 
+// Sparse pass, rank-ordered stream: inv[h, rank[h, j]] = j for ranks in [0, S).
+__global__ void rank_inverse_kernel(const int32_t* __restrict__ ranks, int S, long long total,
+                                    int32_t* __restrict__ inv) {
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (long long)gridDim.x * blockDim.x) {
+    const long long h = e / S;
+    const int r = ranks[e];
+    if ((unsigned)r < (unsigned)S) inv[h * S + r] = (int)(e - h * S);
+  }
+}
+
+// Keys in rank order, ks[h, r] = k[h, inv[h, r]], and a check that inv is the inverse of a
+// permutation (every rank has a position whose rank is that rank); *ok becomes 0 otherwise.
+__global__ void gather_rank_order_kernel(const uint4* __restrict__ k, const int32_t* __restrict__ ranks,
+                                         const int32_t* __restrict__ inv, int S, int vpr,
+                                         long long total, uint4* __restrict__ ks, int* ok) {
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (long long)gridDim.x * blockDim.x) {
+    const long long hr = e / vpr;
+    const int c = (int)(e - hr * vpr);
+    const long long h = hr / S;
+    const int r = (int)(hr - h * S);
+    const int j = inv[hr];
+    const bool valid = j >= 0 && j < S && ranks[h * S + j] == r;
+    if (!valid && c == 0) *ok = 0;
+    ks[e] = valid ? k[(h * S + j) * vpr + c] : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 __global__ void __launch_bounds__(BM) fam_reduce_kernel(const float* __restrict__ part, int S, int NT0,
                                                         int TPC, int CMAX, int NKT,
                                                         float* __restrict__ F) {
@@ -680,6 +792,12 @@ cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
 
 }  // namespace
 
+size_t sparse_lse_workspace_size(int dtype, AttnShape s) {
+  if (!tc_supported(dtype, s)) return 0;
+  const size_t n = (size_t)s.n_batch * s.h_kv * s.seq_len;
+  return ((n * 4 + 255) & ~(size_t)255) + ((n * HD * 2 + 255) & ~(size_t)255) + 256;
+}
+
 bool tc_supported(int dtype, AttnShape s) {
   return (dtype == KVP_BF16 || dtype == KVP_F16) && s.head_dim == HD && encode_fn() != nullptr;
 }
@@ -718,7 +836,33 @@ cudaError_t launch_lse_tc(const void* q, const void* k, int dtype, AttnShape s, 
     p.n_sink = mask->n_sink;
     p.window = mask->window;
     p.ranks_vec = s.seq_len % 4 == 0 && ((uintptr_t)mask->ranks & 15) == 0;
-    return launch_tc<2>(tq, tk, tk, p, p.n_groups * p.NQT, dtype == KVP_BF16, st);
+    if (!mask->inv) return launch_tc<2>(tq, tk, tk, p, p.n_groups * p.NQT, dtype == KVP_BF16, st);
+    // rank-ordered stream: inverse permutation, keys in rank order, validity flag
+    const int BHkv = s.n_batch * s.h_kv;
+    const long long n = (long long)BHkv * s.seq_len;
+    cudaError_t e = cudaMemsetAsync(mask->inv, 0xFF, (size_t)n * sizeof(int32_t), st);
+    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(mask->perm_ok, 1, sizeof(int), st);      // nonzero until a check fails
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long cap = (long long)sms * 8;
+    const int vpr = HD * 2 / 16;
+    long long b1 = (n + 255) / 256, b2 = (n * vpr + 255) / 256;
+    b1 = b1 > cap ? cap : b1;
+    b2 = b2 > cap ? cap : b2;
+    count_launches(2);
+    rank_inverse_kernel<<<(unsigned)b1, 256, 0, st>>>(mask->ranks, s.seq_len, n, mask->inv);
+    gather_rank_order_kernel<<<(unsigned)b2, 256, 0, st>>>((const uint4*)k, mask->ranks, mask->inv, s.seq_len,
+                                                           vpr, n * vpr, (uint4*)mask->k_sorted, mask->perm_ok);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    CUtensorMap tks;
+    if (!make_tmap(&tks, mask->k_sorted, dtype, BHkv, s.seq_len)) return cudaErrorInvalidValue;
+    p.inv = mask->inv;
+    p.perm_ok = mask->perm_ok;
+    return launch_tc<2>(tq, tk, tks, p, p.n_groups * p.NQT, dtype == KVP_BF16, st);
   }
   return launch_tc<0>(tq, tk, tk, p, p.n_groups * p.NQT, dtype == KVP_BF16, st);
 }

@@ -165,9 +165,16 @@ int kvp_topk_cutoffs(const int32_t* ranks, int n_heads, int seq_len, int n_sink,
   return KVP_OK;
 }
 
+size_t kvp_sparse_lse_workspace_size(int dtype, int n_batch, int h_q, int h_kv, int seq_len, int head_dim) {
+  if (check_dtype(dtype) != KVP_OK || check_attn_shape(n_batch, h_q, h_kv, seq_len, head_dim) != KVP_OK)
+    return 0;
+  return kvp::sparse_lse_workspace_size(dtype, kvp::AttnShape{n_batch, h_q, h_kv, seq_len, head_dim});
+}
+
 int kvp_sparse_lse_pass(const void* q, const void* k, const int32_t* ranks, const int32_t* tau,
                         int dtype, int n_batch, int h_q, int h_kv, int seq_len, int head_dim,
-                        float sm_scale, int n_sink, int window, float* lse, kvp_stream_t stream) {
+                        float sm_scale, int n_sink, int window, float* lse, void* workspace,
+                        size_t workspace_bytes, kvp_stream_t stream) {
   g_last_error.clear();
   KVP_TRY(check_dtype(dtype));
   KVP_TRY(check_attn_shape(n_batch, h_q, h_kv, seq_len, head_dim));
@@ -178,7 +185,18 @@ int kvp_sparse_lse_pass(const void* q, const void* k, const int32_t* ranks, cons
   int* st = nullptr;
   KVP_TRY(status_ptr(&st));
   kvp::AttnShape s{n_batch, h_q, h_kv, seq_len, head_dim};
-  const kvp::SparseMask mask{ranks, tau, n_sink, window};
+  kvp::SparseMask mask{ranks, tau, n_sink, window};
+  const size_t need = kvp::sparse_lse_workspace_size(dtype, s);
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need)
+      return fail(KVP_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+    if (((uintptr_t)workspace & 255) != 0) return fail(KVP_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+    const size_t n = (size_t)n_batch * h_kv * seq_len;
+    char* w = (char*)workspace;
+    mask.inv = (int32_t*)w;
+    mask.k_sorted = w + ((n * 4 + 255) & ~(size_t)255);
+    mask.perm_ok = (int*)(w + ((n * 4 + 255) & ~(size_t)255) + ((n * 128 * 2 + 255) & ~(size_t)255));
+  }
   cudaError_t e = kvp::tc_supported(dtype, s)
                       ? kvp::launch_lse_tc(q, k, dtype, s, sm_scale, lse, st, (cudaStream_t)stream, &mask)
                       : kvp::launch_lse_simt(q, k, dtype, s, sm_scale, lse, (cudaStream_t)stream, &mask);

@@ -20,7 +20,14 @@ struct SparseMask {
   const int32_t* ranks;
   const int32_t* tau;
   int n_sink, window;
+  // Tensor-core path only (null: dense streaming): workspace for the rank-ordered key stream --
+  // the inverse permutation [n_batch*h_kv, S], the keys in rank order, a validity flag.
+  int32_t* inv = nullptr;
+  void* k_sorted = nullptr;
+  int* perm_ok = nullptr;
 };
+// Workspace of the sparse row LSE on the tensor-core path (0 for the fp32 path).
+size_t sparse_lse_workspace_size(int dtype, AttnShape s);
 
 // fp32-FFMA tiled passes (any dtype; the only path for float32 inputs).  mask != null: the
 // sparse row LSE.

@@ -132,3 +132,29 @@ def test_sparse_lse_qwen3_8b_131k_sampled(kvp):
     want = oracle.sparse_row_lse(q[0].cpu(), k[0].cpu(), ranks.cpu().numpy(), want_tau[None],
                                  w.head_dim ** -0.5, w.n_sink, w.window, rows=rows)
     check_lse(np64(lse[0])[:, rows], want, "131k sparse LSE")
+
+
+def test_sparse_lse_any_cutoffs_and_ranks(kvp):
+    """The mask is applied as written: cutoffs that are not monotone (drawn at random) with valid
+    ranks (the rank-ordered stream must cover every row's cutoff), and ranks that are not a
+    permutation (the pass falls back to the dense stream)."""
+    S, Hq, Hkv, D, s, w = 1024, 4, 2, 128, 4, 32
+    gen = torch.Generator().manual_seed(77)
+    q = torch.randn(1, Hq, S, D, generator=gen).to(torch.bfloat16)
+    kk = torch.randn(1, Hkv, S, D, generator=gen).to(torch.bfloat16)
+    ranks = kvp_inputs.make_static_ranks(Hkv, S, seed=5)
+    tau = torch.randint(100, 400, (Hkv, S), generator=gen).to(torch.int32)
+    tau[:, :200] = -1
+    lse = kvp.kvp_sparse_lse_pass(q.cuda(), kk.cuda(), ranks.cuda(), tau.cuda(), s, w)
+    torch.cuda.synchronize()
+    kvp.kvp_check_device_status()
+    want = oracle.sparse_row_lse(q[0], kk[0], ranks.numpy(), tau.numpy(), D ** -0.5, s, w)
+    check_lse(np64(lse[0]), want, "random cutoffs")
+    bad = ranks.clone()
+    bad[0, 10] = bad[0, 20]                      # not a permutation
+    tau2 = torch.full((Hkv, S), 300, dtype=torch.int32)
+    lse2 = kvp.kvp_sparse_lse_pass(q.cuda(), kk.cuda(), bad.cuda(), tau2.cuda(), s, w)
+    torch.cuda.synchronize()
+    kvp.kvp_check_device_status()
+    want2 = oracle.sparse_row_lse(q[0], kk[0], bad.numpy(), tau2.numpy(), D ** -0.5, s, w)
+    check_lse(np64(lse2[0]), want2, "ranks not a permutation")
