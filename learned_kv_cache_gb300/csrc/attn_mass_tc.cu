@@ -23,7 +23,7 @@
 //    i >= j + w; queries past S get lse = +inf (weight 0).
 //
 // CTA layout (320 threads, 2 CTAs per SM): warps 0-7 epilogue (warp w reads
-// TMEM lanes 32*(w%4).., columns half w/4 of each tile), warp 8 TMA producer,
+// TMEM lanes 32*(w%4).., column half w/4 of each tile), warp 8 TMA producer,
 // warp 9 TMEM allocator + MMA issuer (one elected thread).  Shared memory:
 // A tile (32 KB) + 2 B stages (2 x 32 KB); TMEM: 2 accumulators of 128 fp32
 // columns so the MMA of tile t+1 overlaps the epilogue of tile t.
@@ -52,10 +52,19 @@ constexpr int BN = 128;            // rows of a streamed B tile (TMEM columns pe
 constexpr int HD = 128;            // head dim (MMA K)
 constexpr int NSTAGE = 2;          // B tiles in flight
 constexpr int NACC = 2;            // TMEM accumulators
-constexpr int EPI_WARPS = 8;
-constexpr int PRODUCER_WARP = 8;
-constexpr int MMA_WARP = 9;
-constexpr int THREADS = 32 * (EPI_WARPS + 2);
+
+// Epilogue layout: warp w reads TMEM lanes 32*(w%4).. and column group w/4 of each tile (NCG
+// groups of CW columns).  Two groups (8 warps) measured faster than four (16 warps of 32 columns,
+// where the per-tile overhead doubles) for every pass.
+template <int MODE>
+struct Epi {
+  static constexpr int NCG = 2;
+  static constexpr int WARPS = 4 * NCG;
+  static constexpr int CW = BN / NCG;
+  static constexpr int PRODUCER = WARPS;
+  static constexpr int MMA = WARPS + 1;
+  static constexpr int THREADS = 32 * (WARPS + 2);
+};
 constexpr int TILE_BYTES = 128 * HD * 2;         // 32 KB: two 128-row x 128-byte halves
 constexpr int HALF_BYTES = TILE_BYTES / 2;
 constexpr int TMEM_COLS = NACC * BN;             // 256
@@ -74,7 +83,11 @@ constexpr int OFF_RED = OFF_BEXT + NSTAGE * EXT_BYTES;
 constexpr int NRK = 8;
 constexpr int OFF_RANK = OFF_AEXT;
 static_assert(NRK * BN * 4 <= OFF_RED - OFF_AEXT, "rank ring must fit in the extension area");
-constexpr int SMEM_BYTES = OFF_RED + 2 * BM * 4 + 1024;   // + alignment slack
+// Row-state exchange of the epilogue (NCG - 1 groups of [m | l] per row).
+template <int MODE>
+__host__ __device__ constexpr int off_red() { return OFF_RED; }
+template <int MODE>
+constexpr int smem_bytes() { return off_red<MODE>() + (Epi<MODE>::NCG - 1) * 2 * BM * 4 + 1024; }   // + alignment slack
 
 // Byte offset of element (r, k) of a [128 x 16] K-major operand in 8 x 16-byte core matrices
 // (core (r/8, k/8) at (r/8)*256 + (k/8)*128): the layout desc_noswz(addr, 128, 256) reads.
@@ -200,7 +213,7 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(THREADS, 2)
+__global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmE, const TcParams p, const bool bf16) {
   extern __shared__ uint8_t smem_raw[];
@@ -217,7 +230,9 @@ __global__ void __launch_bounds__(THREADS, 2)
   int* rbuf = reinterpret_cast<int*>(smem + OFF_RANK);         // [NRK][BN]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
-  float* red = reinterpret_cast<float*>(smem + OFF_RED);
+  float* red = reinterpret_cast<float*>(smem + off_red<MODE>());
+  constexpr int EPI_WARPS = Epi<MODE>::WARPS, PRODUCER_WARP = Epi<MODE>::PRODUCER, MMA_WARP = Epi<MODE>::MMA;
+  constexpr int NCG = Epi<MODE>::NCG, CW = Epi<MODE>::CW;
   const uint32_t sAext = s_base + OFF_AEXT;
   const uint32_t sBext = s_base + OFF_BEXT;
 
@@ -427,7 +442,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int half = warp >> 2, quad = warp & 3;
+    const int half = warp >> 2, quad = warp & 3;   // column group, TMEM lane quarter
     const int r = quad * 32 + lane;            // row of the A tile handled by this thread
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     uint64_t acc01 = 0, acc23 = 0;                           // mass pass: packed fp32 pairs
@@ -444,13 +459,12 @@ __global__ void __launch_bounds__(THREADS, 2)
       const int a = t % NACC;
       if (!ptx::mbar_wait(bar_accf + 8 * a, (t / NACC) & 1, abort_flag, p.status)) { ok = false; break; }
       ptx::tc_fence_after();
-      uint32_t v[64];
+      uint32_t v[CW];
       {
-        uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
-        uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
-        const uint32_t taddr = tmem + lane_base + a * BN + half * 64;
-        ptx::tmem_ld32(taddr, v0);
-        ptx::tmem_ld32(taddr + 32, v1);
+        const uint32_t taddr = tmem + lane_base + a * BN + half * CW;
+#pragma unroll
+        for (int h = 0; h < CW / 32; ++h)
+          ptx::tmem_ld32(taddr + 32 * h, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * h]));
         ptx::tmem_ld_wait();
       }
       ptx::tc_fence_before();
@@ -462,8 +476,8 @@ __global__ void __launch_bounds__(THREADS, 2)
         const bool diag = (kt == it.tile);
         if (diag) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (half * 64 + c > r) v[c] = __float_as_uint(-INFINITY);
+          for (int c = 0; c < CW; ++c)
+            if (half * CW + c > r) v[c] = __float_as_uint(-INFINITY);
         }
         if (MODE == 2 && rank_mode && kt < 0) {
           // rank-ordered tile: column c holds the key of rank rb + c at position pos[c]; kept
@@ -472,11 +486,11 @@ __global__ void __launch_bounds__(THREADS, 2)
             ok = false;
             break;
           }
-          const int* ps = rbuf + (t % NRK) * BN + half * 64;
-          const int cmax = tau_eff - ((t - n_pos) * BN + half * 64);   // rank within the cutoff: c <= cmax
+          const int* ps = rbuf + (t % NRK) * BN + half * CW;
+          const int cmax = tau_eff - ((t - n_pos) * BN + half * CW);   // rank within the cutoff: c <= cmax
           const int span = row_i - p.window - p.n_sink;                // eligible: 0 <= pos - n_sink <= span
 #pragma unroll
-          for (int g4 = 0; g4 < 16; ++g4) {
+          for (int g4 = 0; g4 < CW / 4; ++g4) {
             const int4 p4 = *reinterpret_cast<const int4*>(ps + 4 * g4);
             const int c = 4 * g4;
             const int d0 = p4.x - p.n_sink, d1 = p4.y - p.n_sink, d2 = p4.z - p.n_sink, d3 = p4.w - p.n_sink;
@@ -490,19 +504,19 @@ __global__ void __launch_bounds__(THREADS, 2)
           // are dropped when their rank is past the row's cutoff.  (The sink and window tiles of
           // the rank-ordered plan carry rank +inf: their eligible keys are counted by the
           // rank-ordered tiles.)
-          const int jb = kt * BN + half * 64;
+          const int jb = kt * BN + half * CW;
           const int cw = row_i - p.window - jb, cs = p.n_sink - jb;
-          const int lo = cs > 0 ? cs : 0, hi = cw < 63 ? cw : 63;
+          const int lo = cs > 0 ? cs : 0, hi = cw < CW - 1 ? cw : CW - 1;
           if (__any_sync(0xffffffffu, tau_eff != INT_MAX && lo <= hi)) {
             if (!ptx::mbar_wait(bar_rk + 8 * (t % NRK), (t / NRK) & 1, abort_flag, p.status)) {
               ok = false;
               break;
             }
-            const int* rk = rbuf + (t % NRK) * BN + half * 64;
-            if (__all_sync(0xffffffffu, lo == 0 && hi == 63)) {
+            const int* rk = rbuf + (t % NRK) * BN + half * CW;
+            if (__all_sync(0xffffffffu, lo == 0 && hi == CW - 1)) {
               // every column eligible for every row of the warp: the rank test alone
 #pragma unroll
-              for (int g4 = 0; g4 < 16; ++g4) {
+              for (int g4 = 0; g4 < CW / 4; ++g4) {
                 const int4 r4 = *reinterpret_cast<const int4*>(rk + 4 * g4);
                 v[4 * g4 + 0] = r4.x > tau_eff ? 0xff800000u : v[4 * g4 + 0];
                 v[4 * g4 + 1] = r4.y > tau_eff ? 0xff800000u : v[4 * g4 + 1];
@@ -511,7 +525,7 @@ __global__ void __launch_bounds__(THREADS, 2)
               }
             } else {
 #pragma unroll
-              for (int g4 = 0; g4 < 16; ++g4) {
+              for (int g4 = 0; g4 < CW / 4; ++g4) {
                 const int4 r4 = *reinterpret_cast<const int4*>(rk + 4 * g4);
                 const int rr[4] = {r4.x, r4.y, r4.z, r4.w};
 #pragma unroll
@@ -523,41 +537,76 @@ __global__ void __launch_bounds__(THREADS, 2)
             }
           }
         }
-        float tm = -INFINITY;
+        // sum over the tile of exp2(c2 * s - mref), four independent packed chains
+        auto tile_sum = [&](float mref) -> float {
+          const uint64_t nm2 = pack2(-mref, -mref);
+          uint64_t s0 = 0, s1 = 0, s2 = 0, s3 = 0;
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) tm = max3(tm, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
-        const float mn = fmaxf(m, tm * p.c2);
-        if (mn == -INFINITY) continue;
-        if (mn > m) {
-          l *= fast_exp2(m - mn);
-          m = mn;
+          for (int c = 0; c < CW; c += 8) {
+            float x0, x1, x2, x3, x4, x5, x6, x7;
+            unpack2(ffma2(pack2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), c2x2, nm2), x0, x1);
+            unpack2(ffma2(pack2(__uint_as_float(v[c + 2]), __uint_as_float(v[c + 3])), c2x2, nm2), x2, x3);
+            unpack2(ffma2(pack2(__uint_as_float(v[c + 4]), __uint_as_float(v[c + 5])), c2x2, nm2), x4, x5);
+            unpack2(ffma2(pack2(__uint_as_float(v[c + 6]), __uint_as_float(v[c + 7])), c2x2, nm2), x6, x7);
+            s0 = fadd2(s0, pack2(fast_exp2(x0), fast_exp2(x1)));
+            s1 = fadd2(s1, pack2(fast_exp2(x2), fast_exp2(x3)));
+            s2 = fadd2(s2, pack2(fast_exp2(x4), fast_exp2(x5)));
+            s3 = fadd2(s3, pack2(fast_exp2(x6), fast_exp2(x7)));
+          }
+          float q0, q1, q2, q3;
+          unpack2(fadd2(s0, s1), q0, q1);
+          unpack2(fadd2(s2, s3), q2, q3);
+          return (q0 + q1) + (q2 + q3);
+        };
+        // Online normaliser against a lazily moved reference m (base 2): once a row has a kept
+        // key the tile is summed against the current m without taking its max; only a sum that
+        // reaches 2^64 (a term near overflow) sends the tile through the exact path (tile max,
+        // rescale of l, sum), and l is brought back below 2^32 by exact power-of-two steps of m.
+        // Terms that underflow against m are below 2^-126 of l >= 1.  (The sparse pass, short of
+        // registers, always takes the exact path.)
+        bool exact = MODE == 2 || m == -INFINITY;
+        if (!exact) {
+          const float ts = tile_sum(m);
+          if (ts < 0x1p64f) {
+            l += ts;
+            if (l >= 0x1p32f) {
+              const int e = (int)((__float_as_uint(l) >> 23) & 0xffu) - 127;
+              l *= __uint_as_float((uint32_t)(127 - e) << 23);
+              m += (float)e;
+            }
+          } else {
+            exact = true;
+          }
         }
-        const uint64_t nm2 = pack2(-m, -m);
-        uint64_t s01 = 0, s23 = 0;
+        if (exact) {
+          float t0 = -INFINITY, t1 = -INFINITY, t2 = -INFINITY, t3 = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) {
-          float x0, x1, x2, x3;
-          unpack2(ffma2(pack2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), c2x2, nm2), x0, x1);
-          unpack2(ffma2(pack2(__uint_as_float(v[c + 2]), __uint_as_float(v[c + 3])), c2x2, nm2), x2, x3);
-          s01 = fadd2(s01, pack2(fast_exp2(x0), fast_exp2(x1)));
-          s23 = fadd2(s23, pack2(fast_exp2(x2), fast_exp2(x3)));
+          for (int c = 0; c < CW; c += 8) {
+            t0 = max3(t0, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+            t1 = max3(t1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+            t2 = max3(t2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
+            t3 = max3(t3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
+          }
+          const float mn = fmaxf(m, fmaxf(fmaxf(t0, t1), fmaxf(t2, t3)) * p.c2);
+          if (mn == -INFINITY) continue;
+          if (mn > m) {
+            l *= fast_exp2(m - mn);
+            m = mn;
+          }
+          l += tile_sum(m);
         }
-        float q0, q1, q2, q3;
-        unpack2(s01, q0, q1);
-        unpack2(s23, q2, q3);
-        l += (q0 + q1) + (q2 + q3);
       } else {
         // the accumulator holds (q.k - lse_i/scale); past S it is -inf
         const int u = t % it.per_head;
         const bool diag = (it.chunk == 0 && u == 0);
         if (diag) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (half * 64 + c < r) v[c] = __float_as_uint(-INFINITY);
+          for (int c = 0; c < CW; ++c)
+            if (half * CW + c < r) v[c] = __float_as_uint(-INFINITY);
         }
         const uint64_t zero2 = 0;
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) {
+        for (int c = 0; c < CW; c += 4) {
           float x0, x1, x2, x3;
           unpack2(ffma2(pack2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), c2x2, zero2), x0, x1);
           unpack2(ffma2(pack2(__uint_as_float(v[c + 2]), __uint_as_float(v[c + 3])), c2x2, zero2), x2, x3);
@@ -580,17 +629,24 @@ __global__ void __launch_bounds__(THREADS, 2)
     // Combine the two column halves of every row and write the result.
     asm volatile("bar.sync 1, %0;" ::"r"(EPI_WARPS * 32));
     if (MODE != 1) {
-      if (half == 1) {
-        red[r] = m;
-        red[BM + r] = l;
+      if (half > 0) {
+        red[(half - 1) * 2 * BM + r] = m;
+        red[(half - 1) * 2 * BM + BM + r] = l;
       }
       asm volatile("bar.sync 1, %0;" ::"r"(EPI_WARPS * 32));
       if (half == 0 && ok && !*abort_flag) {
-        const float m1 = red[r], l1 = red[BM + r];
-        const float M = fmaxf(m, m1);
+        float M = m;
+#pragma unroll
+        for (int g = 1; g < NCG; ++g) M = fmaxf(M, red[(g - 1) * 2 * BM + r]);
         float L = 0.f;
-        if (M != -INFINITY) L = (m == -INFINITY ? 0.f : l * fast_exp2(m - M)) +
-                                (m1 == -INFINITY ? 0.f : l1 * fast_exp2(m1 - M));
+        if (M != -INFINITY) {
+          L = m == -INFINITY ? 0.f : l * fast_exp2(m - M);
+#pragma unroll
+          for (int g = 1; g < NCG; ++g) {
+            const float mg = red[(g - 1) * 2 * BM + r], lg = red[(g - 1) * 2 * BM + BM + r];
+            if (mg != -INFINITY) L += lg * fast_exp2(mg - M);
+          }
+        }
         const int i = it.tile * BM + r;
         if (i < p.S) p.out[(size_t)it.group * p.S + i] = (M + __log2f(L)) * KVP_LN2;
       }
@@ -783,10 +839,10 @@ template <int MODE>
 cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& te, const TcParams& p,
                       int grid, bool bf16, cudaStream_t st) {
   auto kern = attn_tc_kernel<MODE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<MODE>());
   if (e != cudaSuccess) return e;
   count_launches(1);
-  kern<<<grid, THREADS, SMEM_BYTES, st>>>(tq, tk, te, p, bf16);
+  kern<<<grid, Epi<MODE>::THREADS, smem_bytes<MODE>(), st>>>(tq, tk, te, p, bf16);
   return cudaGetLastError();
 }
 

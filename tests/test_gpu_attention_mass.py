@@ -156,3 +156,27 @@ def test_qwen3_8b_131k_full_size(kvp):
     lse_full[:, rows] = lse_rows
     F_r = oracle.future_attn_mass(qs, ks, lse_full, scale, w.window, keys=keys)
     check_F(np64(F[0, h])[keys][None], F_r, "131k late keys")
+
+
+@pytest.mark.parametrize("step", [3.0, 50.0])
+def test_growing_logits_lse(kvp, step):
+    """Logits that grow along the key axis (natural-log slope `step` per 128 keys): the running
+    normaliser must follow a maximum that keeps rising from tile to tile -- past 2^32 of its
+    reference within a few tiles (step 3) and by more than 2^64 from one tile to the next
+    (step 50, where F of the early keys is far below fp32's range and only the LSE is compared)."""
+    S, Hq = 1100, 4
+    gen = torch.Generator().manual_seed(int(step * 10))
+    scale = 128 ** -0.5
+    a = 8.0
+    q = 0.05 * torch.randn(1, Hq, S, 128, generator=gen)
+    q[..., 0] = a
+    k = 0.05 * torch.randn(1, 1, S, 128, generator=gen)
+    k[..., 0] = step * torch.arange(S, dtype=torch.float32) / (128 * scale * a)
+    q, k = q.to(torch.bfloat16), k.to(torch.bfloat16)
+    lse, F = _run(kvp, q.cuda(), k.cuda(), 16)
+    lse_r = oracle.row_lse(q[0], k[0], scale)
+    assert lse_r[:, -1].min() > (300.0 if step > 10 else 20.0)
+    check_lse(np64(lse[0]), lse_r, f"growing logits step {step}")
+    if step < 10:
+        F_r = oracle.future_attn_mass(q[0], k[0], lse_r, scale, 16)
+        check_F(np64(F[0]), F_r, f"growing logits step {step}")
