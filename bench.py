@@ -47,8 +47,8 @@ NCU_TRAFFIC = {
     # ncu --set full of attn_tc_kernel<1> / <0> on the benchmark layer (S = 8192; the kernel source
     # hashed below), DRAM bytes read + written per launch (profiles/attn_tc_fam_qwen3-4b-layer_S8192.md,
     # profiles/attn_tc_lse_qwen3-4b-layer_S8192.md)
-    "future_attn_mass": {"sha": "0d2ab5c12bfd6edb", "bytes": 134128384 + 3562496},
-    "lse_pass": {"sha": "0d2ab5c12bfd6edb", "bytes": 83912960 + 2407936},
+    "future_attn_mass": {"sha": "e24cbe7dd6c67fc9", "bytes": 133496832 + 3704064},
+    "lse_pass": {"sha": "e24cbe7dd6c67fc9", "bytes": 83913472 + 2443264},
 }
 
 
