@@ -226,7 +226,7 @@ int kvp_rank_rows(const float* scores, int R, int T, int32_t* ranks, void* works
  * normalised cost of a ranking is its auc divided by the auc of
  * kvp_rank_rows(F).  Products and sums are exact to fp64 rounding.
  * workspace: kvp_eviction_auc_workspace_size(R, M, T) bytes (per-chunk partial
- * sums, added in fixed order).  R, M <= 65535.
+ * sums, added in fixed order).  R, M <= 65535 and R * M <= 2^24.
  * ------------------------------------------------------------------------- */
 size_t kvp_eviction_auc_workspace_size(int R, int M, int T);
 int kvp_eviction_auc(const float* F, const int32_t* ranks, int R, int M, int T, double* auc,

@@ -402,7 +402,7 @@ int kvp_rank_rows(const float* scores, int R, int T, int32_t* ranks, void* works
 }
 
 size_t kvp_eviction_auc_workspace_size(int R, int M, int T) {
-  if (R < 1 || R > 65535 || M < 1 || M > 65535 || T < 1) return 0;
+  if (R < 1 || R > 65535 || M < 1 || M > 65535 || (long long)R * M > (1LL << 24) || T < 1) return 0;
   return kvp::eviction_auc_workspace_size(R, M, T);
 }
 
@@ -410,7 +410,7 @@ int kvp_eviction_auc(const float* F, const int32_t* ranks, int R, int M, int T, 
                      void* workspace, size_t workspace_bytes, kvp_stream_t stream) {
   g_last_error.clear();
   if (!F || !ranks || !auc) return fail(KVP_ERR_INVALID_ARG, "null F/ranks/auc");
-  if (R < 1 || R > 65535 || M < 1 || M > 65535 || T < 1)
+  if (R < 1 || R > 65535 || M < 1 || M > 65535 || (long long)R * M > (1LL << 24) || T < 1)
     return fail(KVP_ERR_INVALID_ARG, "R=%d M=%d T=%d", R, M, T);
   const size_t need = kvp::eviction_auc_workspace_size(R, M, T);
   if (!workspace || workspace_bytes < need)

@@ -140,7 +140,9 @@ __global__ void rank_invert_kernel(const int32_t* __restrict__ vals, int R, int 
 // of AUC_CHUNK entries (grid chunk x ranking x row), then a fixed-order sum of the partials.
 // Each product (rank + 1) * F is split exactly into two fp32 numbers (product and its FMA
 // residual; rank + 1 <= 2^24 is exact in fp32) and the terms are added with a compensated
-// (two-sum) fp32 pair, so the fp64 result carries no product rounding and no long-sum drift.
+// (two-sum) fp32 pair, also when the pairs of a warp are combined; fp64 (slow on this part) is
+// used only for the CTA's last sum and the partials, so the result carries no product rounding
+// and no long-sum drift.
 constexpr int AUC_THREADS = 256;
 constexpr int AUC_CHUNK = 8192;
 
@@ -169,26 +171,48 @@ __global__ void __launch_bounds__(AUC_THREADS) auc_partial_kernel(const float* _
     two_sum_add(hi, lo, p);
     lo += e;
   };
-  if (vec) {                                   // rows 16-byte aligned: 4 entries per load
-    for (int t = t0 + 4 * tid; t < t1; t += 4 * AUC_THREADS) {
-      if (t + 3 < t1) {
-        const int4 r4 = __ldg(reinterpret_cast<const int4*>(rk + t));
-        const float4 f4 = __ldg(reinterpret_cast<const float4*>(f + t));
-        add(r4.x, f4.x);
-        add(r4.y, f4.y);
-        add(r4.z, f4.z);
-        add(r4.w, f4.w);
+  if (vec) {                                   // rows 16-byte aligned: 4 entries per load, two loads
+    constexpr int STEP = 4 * AUC_THREADS;      // of each array in flight per thread
+    for (int t = t0 + 4 * tid; t < t1; t += 2 * STEP) {
+      const bool a_full = t + 3 < t1, b_full = t + STEP + 3 < t1;
+      int4 ra = make_int4(0, 0, 0, 0), rb = ra;
+      float4 fa = make_float4(0.f, 0.f, 0.f, 0.f), fb = fa;
+      if (a_full) {
+        ra = __ldg(reinterpret_cast<const int4*>(rk + t));
+        fa = __ldg(reinterpret_cast<const float4*>(f + t));
+      }
+      if (b_full) {
+        rb = __ldg(reinterpret_cast<const int4*>(rk + t + STEP));
+        fb = __ldg(reinterpret_cast<const float4*>(f + t + STEP));
+      }
+      if (a_full) {
+        add(ra.x, fa.x);
+        add(ra.y, fa.y);
+        add(ra.z, fa.z);
+        add(ra.w, fa.w);
       } else {
         for (int u = t; u < t1; ++u) add(__ldg(rk + u), __ldg(f + u));
+      }
+      if (b_full) {
+        add(rb.x, fb.x);
+        add(rb.y, fb.y);
+        add(rb.z, fb.z);
+        add(rb.w, fb.w);
+      } else {
+        for (int u = t + STEP; u < t1; ++u) add(__ldg(rk + u), __ldg(f + u));
       }
     }
   } else {
     for (int t = t0 + tid; t < t1; t += AUC_THREADS) add(__ldg(rk + t), __ldg(f + t));
   }
-  double acc = (double)hi + (double)lo;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if ((tid & 31) == 0) red[tid >> 5] = acc;
+  for (int o = 16; o > 0; o >>= 1) {
+    const float oh = __shfl_xor_sync(0xffffffffu, hi, o);
+    const float ol = __shfl_xor_sync(0xffffffffu, lo, o);
+    two_sum_add(hi, lo, oh);
+    lo += ol;
+  }
+  if ((tid & 31) == 0) red[tid >> 5] = (double)hi + (double)lo;
   __syncthreads();
   if (tid == 0) {
     double s = 0.0;
