@@ -341,13 +341,14 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
     return -1;
   };
   const int j0 = it.tile * BM;     // mass pass: first key of the tile
-  auto b_coords = [&](int t, int& row, int& z) {
+  // mass pass: streamed tile t is query tile u of query head gh of the group (t = gh * per_head + u;
+  // both loops below keep (gh, u) as running counters instead of dividing)
+  auto b_coords = [&](int t, int gh, int u, int& row, int& z) {
     if (MODE != 1) {
       const int kt = key_tile(t);
       row = kt >= 0 ? kt * BN : (t - n_pos) * BN;
       z = kv_z;
     } else {
-      const int gh = t / it.per_head, u = t % it.per_head;
       row = j0 + p.window + BN * (it.chunk * p.TPC + u);
       z = b_of_group * p.Hq + hkv * p.G + gh;
     }
@@ -362,15 +363,20 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
       ptx::tma_load_3d(sA + HALF_BYTES, tmA, bar_a, 64, a_row, a_z);
     }
     if (lane == 0) ptx::prefetch_tmap(&tmE);
-    int t = 0;
+    int t = 0, pgh = 0, pu = 0;
     for (; t < it.n_tiles; ++t) {
       const int s = t % NSTAGE, use = t / NSTAGE;
+      const int gh = pgh, u = pu;
+      if (MODE == 1 && ++pu == it.per_head) {
+        pu = 0;
+        ++pgh;
+      }
       bool ok = true;
       if (use > 0) ok = ptx::mbar_wait(bar_empty + 8 * s, (use - 1) & 1, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, ok)) break;
       if (lane == 0) {
         int row, z;
-        b_coords(t, row, z);
+        b_coords(t, gh, u, row, z);
         const uint32_t dst = sB + s * TILE_BYTES;
         // Mass pass: the stage also receives the 128 query rows' -lse/scale extension (three
         // 16-bit parts per row, prepared in global memory) by its own TMA box.
@@ -455,8 +461,14 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
     }
     bool ok = true;
     const uint64_t c2x2 = pack2(p.c2, p.c2);
+    int egh = 0, eu = 0;                                     // mass pass: (query head, tile) of t
     for (int t = 0; t < it.n_tiles; ++t) {
       const int a = t % NACC;
+      const int gh = egh, u = eu;
+      if (MODE == 1 && ++eu == it.per_head) {
+        eu = 0;
+        ++egh;
+      }
       if (!ptx::mbar_wait(bar_accf + 8 * a, (t / NACC) & 1, abort_flag, p.status)) { ok = false; break; }
       ptx::tc_fence_after();
       uint32_t v[CW];
@@ -597,7 +609,6 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
         }
       } else {
         // the accumulator holds (q.k - lse_i/scale); past S it is -inf
-        const int u = t % it.per_head;
         const bool diag = (it.chunk == 0 && u == 0);
         if (diag) {
 #pragma unroll
@@ -617,7 +628,6 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
           float f0, f1, f2, f3;
           unpack2(acc01, f0, f1);
           unpack2(acc23, f2, f3);
-          const int gh = t / it.per_head;
           float* dst = p.out + ((((size_t)it.group * p.NKT + it.tile) * p.CMAX + it.chunk) * p.G + gh) * 2 * BM;
           dst[half * BM + r] = (f0 + f1) + (f2 + f3);
           acc01 = 0;
