@@ -218,8 +218,14 @@ __global__ void __launch_bounds__(DM_THREADS, 2)
       ptx::prefetch_tmap(&tmK);
       ptx::prefetch_tmap(&tmV);
       int li = 0;
+      // (row, tile) of x as running counters (one division for the start of the range)
+      int rr = (int)(x_begin / p.NT), uu = (int)(x_begin - (long long)rr * p.NT);
       for (long long x = x_begin; x < x_end; ++x) {
-        const int r = (int)(x / p.NT), u = (int)(x % p.NT);
+        const int r = rr, u = uu;
+        if (++uu == p.NT) {
+          uu = 0;
+          ++rr;
+        }
         // The first tile of the range is copied without waiting for the row length (it is
         // inside the cache whatever the length); the consumers release it unread if it is
         // past the end of the row.
@@ -385,8 +391,13 @@ __global__ void __launch_bounds__(DM_THREADS, 2)
       ++seg;
     };
 
+    int rr = first_row, uu = (int)(x_begin - (long long)first_row * p.NT);
     for (long long x = x_begin; x < x_end; ++x) {
-      const int r = (int)(x / p.NT), u = (int)(x % p.NT);
+      const int r = rr, u = uu;
+      if (++uu == p.NT) {
+        uu = 0;
+        ++rr;
+      }
       if (r != cur_row) {
         if (cur_row >= 0) finish_row(cur_row);
         cur_row = r;
