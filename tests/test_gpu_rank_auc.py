@@ -69,3 +69,21 @@ def test_eviction_auc_from_future_mass(kvp):
             want = oracle.eviction_auc(Fn[r], rand[r, m].cpu().numpy())
             assert abs(auc[r, m].item() - want) <= 1e-9 * want
             assert auc[r, m].item() >= auc_opt[r, 0].item()
+
+
+@pytest.mark.parametrize("R,M,T", [(2, 3, 1), (1, 2, 8191), (3, 5, 20003), (2, 4, 16388)])
+def test_eviction_auc_shapes(kvp, R, M, T):
+    """Scalar path (T not a multiple of 4), several 8192-entry chunks with a ragged tail, the
+    vector path with a 4-entry tail chunk, a single entry; F spans many binades."""
+    gen = torch.Generator(device="cuda").manual_seed(R * 1000 + T)
+    F = torch.exp(4.0 * torch.randn(R, T, generator=gen, device="cuda")) * 1e-3
+    rk = torch.stack([torch.stack([torch.randperm(T, generator=gen, device="cuda") for _ in range(M)])
+                      for _ in range(R)]).to(torch.int32).contiguous()
+    auc = kvp.kvp_eviction_auc(F, rk)
+    torch.cuda.synchronize()
+    kvp.kvp_check_device_status()
+    Fn = F.cpu().numpy().astype(np.float64)
+    for r in range(R):
+        for m in range(M):
+            want = oracle.eviction_auc(Fn[r], rk[r, m].cpu().numpy())
+            assert abs(auc[r, m].item() - want) <= 1e-9 * want, (r, m, auc[r, m].item(), want)
