@@ -705,32 +705,27 @@ __global__ void ext_prep_kernel(const float* __restrict__ lse, int BHq, int S, i
   }
 }
 
-// Sparse pass, rank-ordered stream: inv[h, rank[h, j]] = j for ranks in [0, S).
-__global__ void rank_inverse_kernel(const int32_t* __restrict__ ranks, int S, long long total,
-                                    int32_t* __restrict__ inv) {
-  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
-       e += (long long)gridDim.x * blockDim.x) {
-    const long long h = e / S;
-    const int r = ranks[e];
-    if ((unsigned)r < (unsigned)S) inv[h * S + r] = (int)(e - h * S);
-  }
-}
+// Sparse pass, rank-ordered stream, in one scatter over the keys: inv[h, rank[h, j]] = j and
+// ks[h, rank[h, j]] = k[h, j].  inv starts at -1; a rank outside [0, S) or a rank met twice (the
+// previous inv entry was already set) clears *ok.  S in-range ranks without a repeat are a
+// permutation, so *ok stays nonzero exactly when ks and inv are complete.
+constexpr int RS_VPR = HD * 2 / 16;        // 16-byte vectors per key row
 
-// Keys in rank order, ks[h, r] = k[h, inv[h, r]], and a check that inv is the inverse of a
-// permutation (every rank has a position whose rank is that rank); *ok becomes 0 otherwise.
-__global__ void gather_rank_order_kernel(const uint4* __restrict__ k, const int32_t* __restrict__ ranks,
-                                         const int32_t* __restrict__ inv, int S, int vpr,
-                                         long long total, uint4* __restrict__ ks, int* ok) {
+__global__ void rank_scatter_keys_kernel(const uint4* __restrict__ k, const int32_t* __restrict__ ranks,
+                                         int S, long long total, int32_t* __restrict__ inv,
+                                         uint4* __restrict__ ks, int* ok) {
   for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
        e += (long long)gridDim.x * blockDim.x) {
-    const long long hr = e / vpr;
-    const int c = (int)(e - hr * vpr);
-    const long long h = hr / S;
-    const int r = (int)(hr - h * S);
-    const int j = inv[hr];
-    const bool valid = j >= 0 && j < S && ranks[h * S + j] == r;
-    if (!valid && c == 0) *ok = 0;
-    ks[e] = valid ? k[(h * S + j) * vpr + c] : make_uint4(0u, 0u, 0u, 0u);
+    const long long hj = e / RS_VPR;                 // h * S + j
+    const int c = (int)(e - hj * RS_VPR);
+    const long long h = hj / S;
+    const int r = ranks[hj];
+    if ((unsigned)r >= (unsigned)S) {
+      if (c == 0) *ok = 0;
+      continue;
+    }
+    if (c == 0 && atomicExch(inv + h * S + r, (int)(hj - h * S)) != -1) *ok = 0;
+    ks[(h * S + r) * RS_VPR + c] = k[e];
   }
 }
 
@@ -914,14 +909,11 @@ cudaError_t launch_lse_tc(const void* q, const void* k, int dtype, AttnShape s, 
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long long cap = (long long)sms * 8;
-    const int vpr = HD * 2 / 16;
-    long long b1 = (n + 255) / 256, b2 = (n * vpr + 255) / 256;
-    b1 = b1 > cap ? cap : b1;
+    long long b2 = (n * RS_VPR + 255) / 256;
     b2 = b2 > cap ? cap : b2;
-    count_launches(2);
-    rank_inverse_kernel<<<(unsigned)b1, 256, 0, st>>>(mask->ranks, s.seq_len, n, mask->inv);
-    gather_rank_order_kernel<<<(unsigned)b2, 256, 0, st>>>((const uint4*)k, mask->ranks, mask->inv, s.seq_len,
-                                                           vpr, n * vpr, (uint4*)mask->k_sorted, mask->perm_ok);
+    count_launches(1);
+    rank_scatter_keys_kernel<<<(unsigned)b2, 256, 0, st>>>((const uint4*)k, mask->ranks, s.seq_len, n * RS_VPR,
+                                                           mask->inv, (uint4*)mask->k_sorted, mask->perm_ok);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     CUtensorMap tks;
