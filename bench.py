@@ -47,8 +47,8 @@ NCU_TRAFFIC = {
     # ncu --set full of attn_tc_kernel<1> / <0> on the benchmark layer (S = 8192; the kernel source
     # hashed below), DRAM bytes read + written per launch (profiles/attn_tc_fam_qwen3-4b-layer_S8192.md,
     # profiles/attn_tc_lse_qwen3-4b-layer_S8192.md)
-    "future_attn_mass": {"sha": "ccf4d7474e8dc28c", "bytes": 133772544 + 3295232},
-    "lse_pass": {"sha": "ccf4d7474e8dc28c", "bytes": 83914240 + 2344192},
+    "future_attn_mass": {"sha": "8928336e781a3540", "bytes": 130244608 + 3129600},
+    "lse_pass": {"sha": "8928336e781a3540", "bytes": 83914240 + 2356736},
 }
 
 
