@@ -8,9 +8,9 @@
 // queries in order.  Here the same cutoffs come from a bitmap over the ranks, and the query
 // axis is cut into chunks that run in parallel:
 //
-//  * a CTA (head, chunk [q0, q0 + 512)) sets the bits of every rank already eligible before
-//    q0 (the static set A) and the per-word prefix counts of that bitmap;
-//  * each of its 8 warps walks 64 of the chunk's queries in order.  The set at query q is A
+//  * a CTA (head, chunk [q0, q0 + 8 * SUB)) sets the bits of every rank already eligible
+//    before q0 (the static set A) and the per-word prefix counts of that bitmap;
+//  * each of its 8 warps walks SUB of the chunk's queries in order.  The set at query q is A
 //    plus the chunk's ranks inserted up to q (a short list with insertion order), so warps
 //    do not interfere.  A warp's first cutoff is found by a binary search on the rank axis
 //    (bitmap prefix count + a count over the list); then inserting a rank above the cutoff
@@ -29,8 +29,10 @@ namespace {
 
 constexpr int CT_WARPS = 8;
 constexpr int CT_THREADS = 32 * CT_WARPS;
-constexpr int CT_SUB = 64;                         // queries walked by one warp
-constexpr int CT_CHUNK = CT_WARPS * CT_SUB;        // queries per CTA
+// Queries walked by one warp (SUB) is a trade: shorter walks finish sooner, but every CTA
+// rebuilds the bitmap of the ranks eligible before its chunk (work ~ S per CTA).  Measured on
+// 8 heads: S = 8192 takes 52 / 29 / 21 us with SUB = 64 / 32 / 16, S = 131072 279 / 359 / 607 us.
+__host__ __device__ constexpr int ct_chunk(int sub) { return CT_WARPS * sub; }
 
 // Largest set bit of the bitmap < limit, or -1 (warp-uniform).
 __device__ __forceinline__ int warp_prev_bit(const uint32_t* bits, int limit, int lane) {
@@ -76,9 +78,11 @@ __device__ __forceinline__ int warp_count_listed(const int* ins, int n, int x) {
   return c;
 }
 
+template <int CT_SUB>
 __global__ void __launch_bounds__(CT_THREADS) cutoff_kernel(const int32_t* __restrict__ ranks, int S,
                                                            int n_sink, int window, int k,
                                                            int32_t* __restrict__ tau, int* status) {
+  constexpr int CT_CHUNK = ct_chunk(CT_SUB);        // queries per CTA
   extern __shared__ uint32_t sm[];
   const int nw = (S + 31) >> 5;
   uint32_t* bits = sm;                                       // [nw] the static set A
@@ -200,18 +204,26 @@ __global__ void __launch_bounds__(CT_THREADS) cutoff_kernel(const int32_t* __res
   if (tid == 0 && bad_sh) raise_status(status, KVP_ERR_DEVICE_CHECK);
 }
 
+template <int SUB>
+cudaError_t launch_cutoffs_sub(const int32_t* ranks, int n_heads, int S, int n_sink, int window, int k,
+                               int32_t* tau, int* status, cudaStream_t st) {
+  const int nw = (S + 31) >> 5;
+  const size_t smem = (2 * (size_t)nw + CT_THREADS + 2 * ct_chunk(SUB)) * 4;
+  cudaError_t e = cudaFuncSetAttribute(cutoff_kernel<SUB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((S + ct_chunk(SUB) - 1) / ct_chunk(SUB), n_heads);
+  count_launches(1);
+  cutoff_kernel<SUB><<<grid, CT_THREADS, smem, st>>>(ranks, S, n_sink, window, k, tau, status);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_topk_cutoffs(const int32_t* ranks, int n_heads, int S, int n_sink, int window,
                                 int k, int32_t* tau, int* status, cudaStream_t st) {
-  const int nw = (S + 31) >> 5;
-  const size_t smem = (2 * (size_t)nw + CT_THREADS + 2 * CT_CHUNK) * 4;
-  cudaError_t e = cudaFuncSetAttribute(cutoff_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  dim3 grid((S + CT_CHUNK - 1) / CT_CHUNK, n_heads);
-  count_launches(1);
-  cutoff_kernel<<<grid, CT_THREADS, smem, st>>>(ranks, S, n_sink, window, k, tau, status);
-  return cudaGetLastError();
+  if (S <= 16384) return launch_cutoffs_sub<16>(ranks, n_heads, S, n_sink, window, k, tau, status, st);
+  if (S <= 65536) return launch_cutoffs_sub<32>(ranks, n_heads, S, n_sink, window, k, tau, status, st);
+  return launch_cutoffs_sub<64>(ranks, n_heads, S, n_sink, window, k, tau, status, st);
 }
 
 }  // namespace kvp

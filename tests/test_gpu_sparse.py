@@ -22,6 +22,7 @@ def kvp():
 @pytest.mark.parametrize("H,S,s,w,k", [
     (3, 1, 0, 0, 1), (2, 100, 4, 16, 8), (2, 1000, 4, 64, 37), (1, 1537, 0, 0, 1),
     (2, 3000, 4, 128, 700), (1, 2048, 2, 5000, 3), (1, 700, 4, 16, 5000), (4, 5001, 4, 64, 1200),
+    (2, 16384, 4, 128, 3000), (1, 20000, 4, 128, 4000), (1, 70001, 4, 128, 9000),
 ])
 def test_cutoffs_match_fenwick_oracle(kvp, H, S, s, w, k):
     ranks = kvp_inputs.make_static_ranks(H, S, seed=S + k)
