@@ -8,9 +8,9 @@
 //
 // Ranking (rank 0 = highest score, ties to the lower index, NaN last, -0.0 == +0.0) is a
 // stable least-significant-digit radix sort of (order key, index) pairs, segmented by row:
-// four 8-bit passes, each a histogram kernel (one CTA per 4096-entry tile), a scan kernel (one
+// four 8-bit passes, each a histogram kernel (one CTA per 2048-entry tile), a scan kernel (one
 // CTA per row: digit-major, tile-minor offsets) and a scatter kernel that ranks a tile's
-// entries stably (16 rounds of 256 in entry order; warp peers by __match_any_sync, counts of
+// entries stably (8 rounds of 256 in entry order; warp peers by __match_any_sync, counts of
 // the earlier warps from shared memory).  A last kernel inverts the sorted order into ranks.
 //
 // AUC: sum over b = 0..T of cost(b) equals sum_t (rank_t + 1) * F_t (each entry is counted
@@ -22,8 +22,8 @@ namespace kvp {
 namespace {
 
 constexpr int RK_THREADS = 256;
-constexpr int RK_PER_THREAD = 16;
-constexpr int RK_TILE = RK_THREADS * RK_PER_THREAD;   // 4096 entries per CTA
+constexpr int RK_PER_THREAD = 8;
+constexpr int RK_TILE = RK_THREADS * RK_PER_THREAD;   // 2048 entries per CTA
 constexpr int RK_WARPS = RK_THREADS / 32;
 
 // Ascending order of the key = descending score; NaN (key ~0) last; -0.0 folded into +0.0.
