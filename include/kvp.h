@@ -178,11 +178,11 @@ int kvp_topk_cutoffs(const int32_t* ranks, int n_heads, int seq_len, int n_sink,
  * (kvp_topk_cutoffs' input and output; any int32 values are accepted, the
  * mask is applied as written).  workspace: kvp_sparse_lse_workspace_size()
  * bytes, 256-byte aligned (0 for the fp32 path).  On the tensor-core path a
- * query tile whose first row has a cutoff streams, instead of every causal
+ * query tile whose rows all have a cutoff streams, instead of every causal
  * key tile, the tiles holding its sinks and windows plus the keys in rank
- * order up to that cutoff (the workspace holds the inverse permutation and
- * the keys in rank order), whenever that is fewer tiles; ranks that are not a
- * permutation fall back to the dense stream.
+ * order up to the largest cutoff of its rows (the workspace holds the inverse
+ * permutation and the keys in rank order), whenever that is fewer tiles;
+ * ranks that are not a permutation fall back to the dense stream.
  * ------------------------------------------------------------------------- */
 size_t kvp_sparse_lse_workspace_size(int dtype, int n_batch, int h_q, int h_kv, int seq_len,
                                      int head_dim);
