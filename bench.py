@@ -719,16 +719,32 @@ def e2e_measure(kvp, x, plan, budgets, w, K, W, stream, flops, ws, dev):
 
 def run_ncu_case(args):
     """A fixed case for profiler captures: `--steps` launches of one stage, no timing.
-    lse / fam / sparse (cutoffs + sparse LSE): one Qwen3-4B-shaped layer at --seq-len (default
-    32768: Q = 256 MiB, larger than L2); decode / select / compact / ring: the Qwen2.5-1.5B decode-eviction shapes (T = 120000,
-    28 layers x 2 KV heads, budget 4096; ring: a full static cache of 4096 slots per row, one
-    insert plus one decode with accumulated key mass per step)."""
+    lse / fam / sparse (cutoffs + sparse LSE) / cutoffs: one Qwen3-4B-shaped layer at --seq-len
+    (default 32768: Q = 256 MiB, larger than L2); decode / select / compact / ring / chunked: the
+    Qwen2.5-1.5B decode-eviction shapes (T = 120000, 28 layers x 2 KV heads, budget 4096; ring: a
+    full static cache of 4096 slots per row, one insert plus one decode with accumulated key mass
+    per step; chunked: two compress steps of 8192-token chunks per step, the second onto the
+    cache); auc: eviction AUC of 16 random rankings per row, 8 rows x 131072."""
     import learned_kv_cache_gb300 as kvp
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     kvp.load()
     case = args.ncu_case
-    if case in ("lse", "fam", "sparse"):
+    if case == "cutoffs":
+        w = kvp_inputs.QWEN3_4B_LAYER.scaled(seq_len=args.seq_len)
+        k_lr = w.budget - w.n_sink - w.window
+        ranks = kvp_inputs.make_static_ranks(w.h_kv, w.seq_len, seed=3, device=dev)
+        tau = kvp.kvp_topk_cutoffs(ranks, w.n_sink, w.window, k_lr)
+        for _ in range(args.steps):
+            kvp.kvp_topk_cutoffs(ranks, w.n_sink, w.window, k_lr, tau=tau)
+    elif case == "auc":
+        w = kvp_inputs.QWEN3_8B_131K
+        R, T, M = w.h_kv, w.seq_len, 16
+        F = torch.rand(R, T, generator=torch.Generator(device=dev).manual_seed(4), device=dev)
+        many = torch.stack([torch.randperm(T, device=dev) for _ in range(R * M)]).view(R, M, T).to(torch.int32)
+        for _ in range(args.steps):
+            kvp.kvp_eviction_auc(F, many)
+    elif case in ("lse", "fam", "sparse"):
         w = kvp_inputs.QWEN3_4B_LAYER.scaled(seq_len=args.seq_len)
         x = kvp_inputs.make_prefill_layer(w, 0, device=dev)
         q, k = x["q"][None].contiguous(), x["k"][None].contiguous()
@@ -782,6 +798,23 @@ def run_ncu_case(args):
             for t in range(args.steps):
                 kvp.kvp_ring_insert(kc, vc, pos, score, fill, nk, nk, b + t, w.n_sink, w.n_recent)
                 kvp.kvp_decode_attn(q, kc, vc, fill, key_mass=score, accumulate=True)
+        elif case == "chunked":
+            # two compress steps per step: the first 8192-token chunk, then the next onto the cache
+            x = kvp_inputs.make_decode_cache(w, device=dev)
+            scores = kvp_inputs.make_scores(R, 2 * 8192, seed=7, device=dev)
+            ck = [x["k"][:, a:a + 8192].contiguous() for a in (0, 8192)]
+            cv = [x["v"][:, a:a + 8192].contiguous() for a in (0, 8192)]
+            cs = [scores[:, a:a + 8192].contiguous() for a in (0, 8192)]
+            del x
+            torch.cuda.empty_cache()           # keep the profiled process's device memory small
+            bufs = [{"k": torch.empty(R, b, D, dtype=ck[0].dtype, device=dev),
+                     "v": torch.empty(R, b, D, dtype=ck[0].dtype, device=dev),
+                     "score": torch.empty(R, b, device=dev),
+                     "pos": torch.empty(R, b, dtype=torch.int32, device=dev)} for _ in range(2)]
+            for _ in range(args.steps):
+                kvp.kvp_chunk_compress(None, 0, ck[0], cv[0], cs[0], 0, b, w.n_sink, w.n_recent, bufs[0])
+                kvp.kvp_chunk_compress(bufs[0], min(8192, max(b, w.n_sink + w.n_recent)), ck[1], cv[1], cs[1],
+                                       8192, b, w.n_sink, w.n_recent, bufs[1])
         else:
             raise SystemExit(f"unknown --ncu-case {case}")
     torch.cuda.synchronize(dev)
@@ -798,7 +831,8 @@ def main():
     ap.add_argument("--impl", default="kvp", choices=["kvp", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ncu-case", default=None,
-                    help="profiler case: lse | fam | decode | select | compact (no JSON line)")
+                    help="profiler case: lse | fam | sparse | cutoffs | decode | select | compact | ring | "
+                         "chunked | auc (no JSON line)")
     ap.add_argument("--seq-len", type=int, default=32768)
     args = ap.parse_args()
     if args.ncu_case:
