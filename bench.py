@@ -703,6 +703,9 @@ def e2e_measure(kvp, x, plan, budgets, w, K, W, stream, flops, ws, dev):
     for _ in range(W):
         step()
     torch.cuda.synchronize(dev)
+    if ws > 1:                             # every rank starts the timed loop together
+        import torch.distributed as dist
+        dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -711,7 +714,7 @@ def e2e_measure(kvp, x, plan, budgets, w, K, W, stream, flops, ws, dev):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     kvp.kvp_check_device_status()
-    ms = e0.elapsed_time(e1) / K
+    ms = reduce_max(e0.elapsed_time(e1) / K, ws, dev)     # the slowest rank sets the time
     return {"value": flops * ws / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "overlap": "H2D in four KV-head slices on a copy stream; each slice's LSE pass starts when it lands, its mass pass on a second compute stream"}
