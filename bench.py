@@ -45,8 +45,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel source is unchanged (sha256 of the .cu file at capture time).
 NCU_TRAFFIC = {
     # ncu --set full of attn_tc_kernel<1> / <0> on the benchmark layer (S = 8192; the kernel source
-    # hashed below), DRAM bytes read + written per launch (profiles/attn_tc_fam_qwen3-4b-layer_S8192.md,
-    # profiles/attn_tc_lse_qwen3-4b-layer_S8192.md)
+    # hashed below), DRAM bytes read + written per launch
     "future_attn_mass": {"sha": "8928336e781a3540", "bytes": 130244608 + 3129600},
     "lse_pass": {"sha": "8928336e781a3540", "bytes": 83914240 + 2356736},
 }

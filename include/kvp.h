@@ -30,9 +30,10 @@
  *   that gave up) are recorded in a per-device status word that
  *   kvp_check_device_status() reads and clears; the affected outputs are then
  *   unspecified.
- * - Tensors are dense and row-major with the last dimension contiguous; the
- *   layout of each argument is given in brackets.  Q/K/V base pointers must be
- *   16-byte aligned.
+ * - Tensors are row-major with the last dimension contiguous; the layout of
+ *   each argument is given in brackets.  They are dense unless the entry point
+ *   takes strides (the Q/K inputs of the attention passes).  Q/K/V base
+ *   pointers must be 16-byte aligned.
  * - head_dim must be 64 or 128.  Logits are scaled by `sm_scale` (normally
  *   1/sqrt(head_dim)); all softmax arithmetic is fp32.
  * - GQA: query head h_q belongs to KV head h_q / (h_q_count / h_kv_count).
@@ -47,7 +48,7 @@
 extern "C" {
 #endif
 
-#define KVP_ABI_VERSION 1
+#define KVP_ABI_VERSION 2
 
 /* A cudaStream_t (struct CUstream_st*), declared without pulling in CUDA headers. */
 typedef struct CUstream_st* kvp_stream_t;
@@ -69,6 +70,26 @@ typedef enum kvp_status {
 } kvp_status;
 
 /* ---------------------------------------------------------------------------
+ * Q / K strides of the attention passes (kvp_lse_pass, kvp_sparse_lse_pass,
+ * kvp_future_attn_mass, kvp_future_attn_target).
+ *
+ * q_strides / k_strides are HOST arrays of three int64 element strides
+ * {batch, head, token} of q and k (the head_dim axis is always contiguous), or
+ * NULL for the dense layout [n_batch, H, seq_len, head_dim].  A slice of a
+ * fused QKV projection [seq_len, (h_q + 2 h_kv) * head_dim] is read in place
+ * with q_strides = {-, head_dim, (h_q + 2 h_kv) * head_dim}.  Every stride
+ * that is used must be a positive multiple of 16 bytes below 2^40 bytes, the
+ * token stride at least head_dim; the stride of an extent-1 dimension (batch
+ * when n_batch = 1, head when there is one head) is ignored.  Outputs (lse, F,
+ * target, F_heads) are always dense.
+ *
+ * Paths: bf16 / f16 inputs run on the tcgen05 tensor-core passes (head_dim 64
+ * or 128, operands loaded by TMA); float32 inputs on the fp32-FFMA passes.
+ * There is no other path: when the driver's tensor-map encoder cannot be
+ * resolved, 16-bit calls fail with KVP_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+
+/* ---------------------------------------------------------------------------
  * A1. Causal row log-sum-exp.
  *
  * KVpop -- Key-Value Cache Compression with Predictive Online Pruning,
@@ -82,9 +103,11 @@ typedef enum kvp_status {
  * lse [n_batch, h_q,  seq_len]            float32, natural log (output)
  * n_batch counts independent problems (e.g. layers).  bf16/f16 inputs run on
  * the tensor cores (fp32 accumulation); float32 inputs on fp32 FFMA.
+ * q_strides / k_strides: see "Q / K strides" above (NULL = dense).
  * ------------------------------------------------------------------------- */
 int kvp_lse_pass(const void* q, const void* k, int dtype, int n_batch, int h_q, int h_kv,
-                 int seq_len, int head_dim, float sm_scale, float* lse, kvp_stream_t stream);
+                 int seq_len, int head_dim, const int64_t* q_strides, const int64_t* k_strides,
+                 float sm_scale, float* lse, kvp_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * A2. Future-attention mass (transposed, key-major column pass).
@@ -99,7 +122,7 @@ int kvp_lse_pass(const void* q, const void* k, int dtype, int n_batch, int h_q, 
  *                exp(sm_scale * q[b, h*G+g, i] . k[b, h, j] - lse[b, h*G+g, i])
  *
  * The S x S matrix is never formed.  Keys j > seq_len - 1 - window get 0.
- * q, k as in kvp_lse_pass; lse is kvp_lse_pass's output.
+ * q, k (and their strides) as in kvp_lse_pass; lse is kvp_lse_pass's output.
  * F [n_batch, h_kv, seq_len] float32 (output).
  * workspace: device scratch of at least kvp_future_attn_mass_workspace_size()
  * bytes (partial sums of long key rows; may be NULL when that size is 0).
@@ -107,9 +130,9 @@ int kvp_lse_pass(const void* q, const void* k, int dtype, int n_batch, int h_q, 
 size_t kvp_future_attn_mass_workspace_size(int dtype, int n_batch, int h_q, int h_kv,
                                            int seq_len, int head_dim, int window);
 int kvp_future_attn_mass(const void* q, const void* k, const float* lse, int dtype, int n_batch,
-                         int h_q, int h_kv, int seq_len, int head_dim, float sm_scale,
-                         int window, float* F, void* workspace, size_t workspace_bytes,
-                         kvp_stream_t stream);
+                         int h_q, int h_kv, int seq_len, int head_dim, const int64_t* q_strides,
+                         const int64_t* k_strides, float sm_scale, int window, float* F,
+                         void* workspace, size_t workspace_bytes, kvp_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * A2'. KVpop's supervision target (per-query-head future mass and its epilogue).
@@ -125,7 +148,7 @@ int kvp_future_attn_mass(const void* q, const void* k, const float* lse, int dty
  *   KVP_TARGET_MAX_LOG:   target[b, h, t] = max_g log(eps + F_g / N_t)
  *   KVP_TARGET_MEAN_PROB: target[b, h, t] = log(eps + (1/G) sum_g F_g / N_t)
  *
- * Inputs as in kvp_future_attn_mass.  Outputs (each nullable, at least one):
+ * Inputs (and strides) as in kvp_future_attn_mass.  Outputs (each nullable, at least one):
  * target [n_batch, h_kv, seq_len] float32; F_heads [n_batch, h_q, seq_len]
  * float32 (the per-query-head mass); F [n_batch, h_kv, seq_len] float32 (their
  * group sum).  eps >= 0 (eps = 0 gives -inf where a key receives no mass);
@@ -137,9 +160,10 @@ int kvp_future_attn_mass(const void* q, const void* k, const float* lse, int dty
 size_t kvp_future_attn_target_workspace_size(int dtype, int n_batch, int h_q, int h_kv,
                                              int seq_len, int head_dim, int window);
 int kvp_future_attn_target(const void* q, const void* k, const float* lse, int dtype, int n_batch,
-                           int h_q, int h_kv, int seq_len, int head_dim, float sm_scale,
-                           int window, float eps, int aggregate, float* target, float* F_heads,
-                           float* F, void* workspace, size_t workspace_bytes, kvp_stream_t stream);
+                           int h_q, int h_kv, int seq_len, int head_dim, const int64_t* q_strides,
+                           const int64_t* k_strides, float sm_scale, int window, float eps,
+                           int aggregate, float* target, float* F_heads, float* F, void* workspace,
+                           size_t workspace_bytes, kvp_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * A1'. Running top-k cutoffs (KVpop's online pruning during prefill/training).
@@ -174,7 +198,7 @@ int kvp_topk_cutoffs(const int32_t* ranks, int n_heads, int seq_len, int n_sink,
  *   lse[b, h, i] = ln sum_{j : keep(i, j)} exp(sm_scale * q[b, h, i] . k[b, h/G, j])
  *
  * tau[i] < 0 (fewer than k eligible tokens) keeps every eligible token.
- * q, k, lse as in kvp_lse_pass; ranks and tau [n_batch, h_kv, seq_len] int32
+ * q, k (and strides), lse as in kvp_lse_pass; ranks and tau [n_batch, h_kv, seq_len] int32
  * (kvp_topk_cutoffs' input and output; any int32 values are accepted, the
  * mask is applied as written).  workspace: kvp_sparse_lse_workspace_size()
  * bytes, 256-byte aligned (0 for the fp32 path).  On the tensor-core path a
@@ -188,8 +212,9 @@ size_t kvp_sparse_lse_workspace_size(int dtype, int n_batch, int h_q, int h_kv, 
                                      int head_dim);
 int kvp_sparse_lse_pass(const void* q, const void* k, const int32_t* ranks, const int32_t* tau,
                         int dtype, int n_batch, int h_q, int h_kv, int seq_len, int head_dim,
-                        float sm_scale, int n_sink, int window, float* lse, void* workspace,
-                        size_t workspace_bytes, kvp_stream_t stream);
+                        const int64_t* q_strides, const int64_t* k_strides, float sm_scale,
+                        int n_sink, int window, float* lse, void* workspace, size_t workspace_bytes,
+                        kvp_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Ranks of score rows (static ranks; the optimal ranking of the eviction cost).
@@ -399,11 +424,19 @@ int kvp_decode_attn(const void* q, const void* kc, const void* vc, int dtype, in
  * nothing and calls no allocating routine.
  *
  * - The first call on each device looks up the scratch array's device
- *   address (a CUDA runtime query, cached per device); make that first call
- *   before capturing any stream on that device.
+ *   address (a CUDA runtime query, cached per device and CUDA context); make
+ *   that first call before capturing any stream on that device.  A first call
+ *   made on a capturing stream is refused with KVP_ERR_INVALID_ARG.
+ * - With lazy module loading (the CUDA default), that first lookup may be the
+ *   moment the library's device code is loaded on the device, and with it the
+ *   fixed array is placed in device memory: the driver's module load, not a
+ *   cudaMalloc by the library, and once per device and context.  After
+ *   cudaDeviceReset the next call runs in a new context and looks the address
+ *   up again.
  * - All calls on a device share the one array and it keeps the last call's
- *   contents; nothing in it needs to start at zero (every partial is written
- *   before it is read).  Calls whose executions overlap on the GPU (different
+ *   contents.  Each call clears, on its stream, what must start at zero (the
+ *   per-row merge counters of the split-K path); every partial is written
+ *   before it is read.  Calls whose executions overlap on the GPU (different
  *   streams, or host threads without ordering) race on the scratch and
  *   produce wrong outputs: serialise them, e.g. on one stream.
  * ------------------------------------------------------------------------- */

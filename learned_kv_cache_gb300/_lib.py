@@ -1,7 +1,8 @@
 """ctypes binding of libkvp.so: the C ABI of include/kvp.h under the same names.
 
 Argument marshalling only: every function checks tensor devices, dtypes,
-shapes and contiguity, passes raw device pointers and the current CUDA stream
+shapes and contiguity (Q/K of the attention passes may be strided views whose
+head_dim axis is contiguous), passes raw device pointers, strides and the current CUDA stream
 to the library, and raises :class:`KvpError` on a non-zero status.  All
 arithmetic runs in the library's CUDA kernels; there is no fallback.
 """
@@ -25,15 +26,16 @@ STATUS = {0: "KVP_OK", -1: "KVP_ERR_INVALID_ARG", -2: "KVP_ERR_UNSUPPORTED", -3:
 _P, _I, _F, _D, _SZ, _I64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_double,
                              ctypes.c_size_t, ctypes.c_int64)
 SIGNATURES = {
-    "kvp_lse_pass": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P]),
+    "kvp_lse_pass": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _F, _P, _P]),
     "kvp_future_attn_mass_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
-    "kvp_future_attn_mass": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _SZ, _P]),
+    "kvp_future_attn_mass": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _F, _I, _P, _P, _SZ, _P]),
     "kvp_future_attn_target_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
-    "kvp_future_attn_target": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _F, _I, _P, _P, _P, _P,
-                                    _SZ, _P]),
+    "kvp_future_attn_target": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _F, _I, _F, _I, _P, _P, _P,
+                                    _P, _SZ, _P]),
     "kvp_topk_cutoffs": (_I, [_P, _I, _I, _I, _I, _I, _P, _P]),
     "kvp_sparse_lse_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
-    "kvp_sparse_lse_pass": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _SZ, _P]),
+    "kvp_sparse_lse_pass": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _F, _I, _I, _P, _P, _SZ,
+                                 _P]),
     "kvp_soft_topk_budgets": (_I, [_P, _I, _D, _I, _P, _P, _P]),
     "kvp_select_topk": (_I, [_P, _I, _I, _I64, _P, _I, _I, _P, _I, _P, _P]),
     "kvp_compact_kv": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P]),
@@ -124,14 +126,30 @@ def _bhsd(q, k):
     return q, k
 
 
+def _strided_input(t: torch.Tensor, name: str, dtype=None, shape=None):
+    """A [B,H,S,D] Q/K view read in place: the head_dim axis must be contiguous; returns the
+    {batch, head, token} element strides as a C int64[3] (None when the view is dense)."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.stride(3) != 1 and t.shape[3] > 1:
+        raise ValueError(f"{name}: the head_dim axis must be contiguous")
+    if t.is_contiguous():
+        return None
+    return (ctypes.c_int64 * 3)(t.stride(0), t.stride(1), t.stride(2))
+
+
 def kvp_lse_pass(q, k, sm_scale=None, lse=None, stream=None):
     """Causal row LSE: q [B,H_q,S,D], k [B,H_kv,S,D] -> lse fp32 [B,H_q,S]."""
     squeeze = q.dim() == 3
     q4, k4 = _bhsd(q, k)
     B, Hq, S, D = q4.shape
     Hkv = k4.shape[1]
-    _need(q4, "q")
-    _need(k4, "k", dtype=q4.dtype, shape=(B, Hkv, S, D))
+    qs = _strided_input(q4, "q")
+    ks = _strided_input(k4, "k", dtype=q4.dtype, shape=(B, Hkv, S, D))
     if sm_scale is None:
         sm_scale = D ** -0.5
     if lse is None:
@@ -139,7 +157,7 @@ def kvp_lse_pass(q, k, sm_scale=None, lse=None, stream=None):
     _need(lse, "lse", torch.float32)
     if lse.numel() != B * Hq * S:
         raise ValueError("lse has the wrong size")
-    rc = load().kvp_lse_pass(_ptr(q4), _ptr(k4), _dtype(q4), B, Hq, Hkv, S, D, float(sm_scale),
+    rc = load().kvp_lse_pass(_ptr(q4), _ptr(k4), _dtype(q4), B, Hq, Hkv, S, D, qs, ks, float(sm_scale),
                              _ptr(lse), _stream(stream))
     _check("kvp_lse_pass", rc)
     return lse[0] if squeeze and lse.dim() == 3 else lse
@@ -172,8 +190,8 @@ def kvp_sparse_lse_pass(q, k, ranks, tau, n_sink, window, sm_scale=None, lse=Non
     q4, k4 = _bhsd(q, k)
     B, Hq, S, D = q4.shape
     Hkv = k4.shape[1]
-    _need(q4, "q")
-    _need(k4, "k", dtype=q4.dtype, shape=(B, Hkv, S, D))
+    qs = _strided_input(q4, "q")
+    ks = _strided_input(k4, "k", dtype=q4.dtype, shape=(B, Hkv, S, D))
     _need(ranks, "ranks", torch.int32)
     _need(tau, "tau", torch.int32)
     if ranks.numel() != B * Hkv * S or tau.numel() != B * Hkv * S:
@@ -190,7 +208,7 @@ def kvp_sparse_lse_pass(q, k, ranks, tau, n_sink, window, sm_scale=None, lse=Non
         workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = load().kvp_sparse_lse_pass(_ptr(q4), _ptr(k4), _ptr(ranks), _ptr(tau), _dtype(q4), B, Hq, Hkv,
-                                    S, D, float(sm_scale), int(n_sink), int(window), _ptr(lse),
+                                    S, D, qs, ks, float(sm_scale), int(n_sink), int(window), _ptr(lse),
                                     _ptr(workspace), ws_bytes, _stream(stream))
     _check("kvp_sparse_lse_pass", rc)
     return lse[0] if squeeze and lse.dim() == 3 else lse
@@ -208,8 +226,8 @@ def kvp_future_attn_mass(q, k, lse, window, sm_scale=None, F=None, workspace=Non
     q4, k4 = _bhsd(q, k)
     B, Hq, S, D = q4.shape
     Hkv = k4.shape[1]
-    _need(q4, "q")
-    _need(k4, "k", dtype=q4.dtype, shape=(B, Hkv, S, D))
+    qs = _strided_input(q4, "q")
+    ks = _strided_input(k4, "k", dtype=q4.dtype, shape=(B, Hkv, S, D))
     _need(lse, "lse", torch.float32)
     if lse.numel() != B * Hq * S:
         raise ValueError("lse has the wrong size")
@@ -225,7 +243,7 @@ def kvp_future_attn_mass(q, k, lse, window, sm_scale=None, F=None, workspace=Non
         workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = load().kvp_future_attn_mass(_ptr(q4), _ptr(k4), _ptr(lse), _dtype(q4), B, Hq, Hkv, S, D,
-                                     float(sm_scale), int(window), _ptr(F), _ptr(workspace),
+                                     qs, ks, float(sm_scale), int(window), _ptr(F), _ptr(workspace),
                                      ws_bytes, _stream(stream))
     _check("kvp_future_attn_mass", rc)
     return F[0] if squeeze and F.dim() == 3 else F
@@ -247,8 +265,8 @@ def kvp_future_attn_target(q, k, lse, window, eps=0.0, aggregate="max_log", sm_s
     q4, k4 = _bhsd(q, k)
     B, Hq, S, D = q4.shape
     Hkv = k4.shape[1]
-    _need(q4, "q")
-    _need(k4, "k", dtype=q4.dtype, shape=(B, Hkv, S, D))
+    qs = _strided_input(q4, "q")
+    ks = _strided_input(k4, "k", dtype=q4.dtype, shape=(B, Hkv, S, D))
     _need(lse, "lse", torch.float32)
     if sm_scale is None:
         sm_scale = D ** -0.5
@@ -265,7 +283,7 @@ def kvp_future_attn_target(q, k, lse, window, eps=0.0, aggregate="max_log", sm_s
         workspace = torch.empty(need, device=dev, dtype=torch.uint8)
     ws_bytes = workspace.numel() * workspace.element_size()
     rc = load().kvp_future_attn_target(_ptr(q4), _ptr(k4), _ptr(lse), _dtype(q4), B, Hq, Hkv, S, D,
-                                       float(sm_scale), int(window), float(eps), agg, _ptr(target),
+                                       qs, ks, float(sm_scale), int(window), float(eps), agg, _ptr(target),
                                        _ptr(F_heads), _ptr(F), _ptr(workspace), ws_bytes,
                                        _stream(stream))
     _check("kvp_future_attn_target", rc)

@@ -1,7 +1,7 @@
 // fp32-FFMA tiled row-LSE and future-attention-mass passes.
 //
-// This is the path for float32 inputs (and a dtype-generic fallback); the
-// bf16/f16 path runs on the tensor cores (attn_mass_tc.cu).  Both passes use
+// This is the path for float32 inputs (the tiny fp32 workload); bf16/f16
+// inputs always run on the tensor cores (attn_mass_tc.cu).  Both passes use
 // the same 64 x 64 register-tiled score block: 256 threads, each owning a
 // 4 x 4 patch, operands staged transposed (feature-major) in shared memory so
 // that every thread reads contiguous float4s.
@@ -25,16 +25,18 @@ constexpr int TM = 64;       // rows per block
 constexpr int TN = 64;       // columns per tile
 constexpr int LD = TM + 4;   // padded leading dimension of the transposed tiles
 
-// Copy rows [r0, r0 + 64) of a [S, D] matrix into sm[d * LD + r] as fp32 (zeros past S).
+// Copy rows [r0, r0 + 64) of a [S, D] matrix (row pitch `pitch` elements) into sm[d * LD + r]
+// as fp32 (zeros past S).
 template <typename T, int D>
-__device__ __forceinline__ void load_tile_t(float* sm, const T* __restrict__ src, int r0, int S) {
+__device__ __forceinline__ void load_tile_t(float* sm, const T* __restrict__ src, int r0, int S,
+                                            long long pitch) {
   constexpr int V = Vec16<T>::N;   // elements per 16-byte vector
   constexpr int VPR = D / V;       // vectors per row
   for (int e = threadIdx.x; e < TM * VPR; e += blockDim.x) {
     const int r = e / VPR, c = (e % VPR) * V;
     float f[V];
     if (r0 + r < S) {
-      const uint4 u = *reinterpret_cast<const uint4*>(src + (size_t)(r0 + r) * D + c);
+      const uint4 u = *reinterpret_cast<const uint4*>(src + (long long)(r0 + r) * pitch + c);
       Vec16<T>::unpack(u, f);
     } else {
 #pragma unroll
@@ -81,7 +83,8 @@ __device__ __forceinline__ float row_sum16(float v) {
 template <typename T, int D>
 __global__ void __launch_bounds__(256) lse_simt_kernel(const T* __restrict__ q,
                                                        const T* __restrict__ k, int Hq, int Hkv,
-                                                       int S, float c2, float* __restrict__ lse,
+                                                       int S, AttnShape sh, float c2,
+                                                       float* __restrict__ lse,
                                                        const int32_t* __restrict__ ranks,
                                                        const int32_t* __restrict__ tau, int n_sink,
                                                        int window) {
@@ -90,10 +93,10 @@ __global__ void __launch_bounds__(256) lse_simt_kernel(const T* __restrict__ q,
   float* Bs = sm + D * LD;
   const int i0 = blockIdx.x * TM, hq = blockIdx.y, b = blockIdx.z;
   const int G = Hq / Hkv;
-  const T* qh = q + (size_t)(b * Hq + hq) * S * D;
-  const T* kh = k + (size_t)(b * Hkv + hq / G) * S * D;
+  const T* qh = q + b * sh.q_sb + hq * sh.q_sh;
+  const T* kh = k + b * sh.k_sb + (hq / G) * sh.k_sh;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  load_tile_t<T, D>(As, qh, i0, S);
+  load_tile_t<T, D>(As, qh, i0, S, sh.q_sr);
   const int32_t* rk = ranks ? ranks + (size_t)(b * Hkv + hq / G) * S : nullptr;
   int tau_r[4];
 #pragma unroll
@@ -108,7 +111,7 @@ __global__ void __launch_bounds__(256) lse_simt_kernel(const T* __restrict__ q,
   const int last = min(S, i0 + TM) - 1;
   for (int j0 = 0; j0 <= last; j0 += TN) {
     __syncthreads();
-    load_tile_t<T, D>(Bs, kh, j0, S);
+    load_tile_t<T, D>(Bs, kh, j0, S, sh.k_sr);
     __syncthreads();
     float acc[4][4];
     tile_dot<D>(As, Bs, ty, tx, acc);
@@ -147,7 +150,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(256) fam_simt_kernel(const T* __restrict__ q,
                                                        const T* __restrict__ k,
                                                        const float* __restrict__ lse, int Hq,
-                                                       int Hkv, int S, float c2, int w,
+                                                       int Hkv, int S, AttnShape sh, float c2, int w,
                                                        float* __restrict__ F, int per_head) {
   extern __shared__ float sm[];
   float* As = sm;
@@ -159,14 +162,14 @@ __global__ void __launch_bounds__(256) fam_simt_kernel(const T* __restrict__ q,
   float f[4] = {0.f, 0.f, 0.f, 0.f};
   const int first = j0 + w;   // first query any key of this block receives
   if (first < S) {
-    load_tile_t<T, D>(As, k + (size_t)(b * Hkv + hk) * S * D, j0, S);
+    load_tile_t<T, D>(As, k + b * sh.k_sb + hk * sh.k_sh, j0, S, sh.k_sr);
     for (int g = 0; g < G; ++g) {
       const int hq = hk * G + g;
-      const T* qh = q + (size_t)(b * Hq + hq) * S * D;
+      const T* qh = q + b * sh.q_sb + hq * sh.q_sh;
       const float* lh = lse + (size_t)(b * Hq + hq) * S;
       for (int i0 = first; i0 < S; i0 += TN) {
         __syncthreads();
-        load_tile_t<T, D>(Bs, qh, i0, S);
+        load_tile_t<T, D>(Bs, qh, i0, S, sh.q_sr);
         if (threadIdx.x < TN) {
           const int i = i0 + threadIdx.x;
           Ls[threadIdx.x] = i < S ? lh[i] * KVP_LOG2E : INFINITY;
@@ -245,7 +248,7 @@ cudaError_t lse_simt(const void* q, const void* k, AttnShape s, float scale, flo
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   dim3 grid((s.seq_len + TM - 1) / TM, s.h_q, s.n_batch);
   count_launches(1);
-  kern<<<grid, 256, smem, st>>>((const T*)q, (const T*)k, s.h_q, s.h_kv, s.seq_len,
+  kern<<<grid, 256, smem, st>>>((const T*)q, (const T*)k, s.h_q, s.h_kv, s.seq_len, s,
                                 scale * KVP_LOG2E, lse, mask ? mask->ranks : nullptr,
                                 mask ? mask->tau : nullptr, mask ? mask->n_sink : 0,
                                 mask ? mask->window : 0);
@@ -260,7 +263,7 @@ cudaError_t fam_simt(const void* q, const void* k, const float* lse, AttnShape s
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   dim3 grid((s.seq_len + TM - 1) / TM, s.h_kv, s.n_batch);
   count_launches(1);
-  kern<<<grid, 256, smem, st>>>((const T*)q, (const T*)k, lse, s.h_q, s.h_kv, s.seq_len,
+  kern<<<grid, 256, smem, st>>>((const T*)q, (const T*)k, lse, s.h_q, s.h_kv, s.seq_len, s,
                                 scale * KVP_LOG2E, w, F, per_head);
   return cudaGetLastError();
 }
@@ -269,28 +272,16 @@ cudaError_t fam_simt(const void* q, const void* k, const float* lse, AttnShape s
 
 cudaError_t launch_lse_simt(const void* q, const void* k, int dtype, AttnShape s, float scale,
                             float* lse, cudaStream_t st, const SparseMask* mask) {
-  const bool d128 = s.head_dim == 128;
-  switch (dtype) {
-    case KVP_F32: return d128 ? lse_simt<float, 128>(q, k, s, scale, lse, st, mask)
-                              : lse_simt<float, 64>(q, k, s, scale, lse, st, mask);
-    case KVP_BF16: return d128 ? lse_simt<__nv_bfloat16, 128>(q, k, s, scale, lse, st, mask)
-                               : lse_simt<__nv_bfloat16, 64>(q, k, s, scale, lse, st, mask);
-    default: return d128 ? lse_simt<__half, 128>(q, k, s, scale, lse, st, mask)
-                         : lse_simt<__half, 64>(q, k, s, scale, lse, st, mask);
-  }
+  if (dtype != KVP_F32) return cudaErrorInvalidValue;    // 16-bit inputs run on the tensor cores
+  return s.head_dim == 128 ? lse_simt<float, 128>(q, k, s, scale, lse, st, mask)
+                           : lse_simt<float, 64>(q, k, s, scale, lse, st, mask);
 }
 
 cudaError_t launch_fam_simt(const void* q, const void* k, const float* lse, int dtype, AttnShape s,
                             float scale, int w, float* F, cudaStream_t st, int per_head) {
-  const bool d128 = s.head_dim == 128;
-  switch (dtype) {
-    case KVP_F32: return d128 ? fam_simt<float, 128>(q, k, lse, s, scale, w, F, st, per_head)
-                              : fam_simt<float, 64>(q, k, lse, s, scale, w, F, st, per_head);
-    case KVP_BF16: return d128 ? fam_simt<__nv_bfloat16, 128>(q, k, lse, s, scale, w, F, st, per_head)
-                               : fam_simt<__nv_bfloat16, 64>(q, k, lse, s, scale, w, F, st, per_head);
-    default: return d128 ? fam_simt<__half, 128>(q, k, lse, s, scale, w, F, st, per_head)
-                         : fam_simt<__half, 64>(q, k, lse, s, scale, w, F, st, per_head);
-  }
+  if (dtype != KVP_F32) return cudaErrorInvalidValue;
+  return s.head_dim == 128 ? fam_simt<float, 128>(q, k, lse, s, scale, w, F, st, per_head)
+                           : fam_simt<float, 64>(q, k, lse, s, scale, w, F, st, per_head);
 }
 
 cudaError_t launch_target_epilogue(const float* F_heads, int n_batch, int h_q, int h_kv, int S,

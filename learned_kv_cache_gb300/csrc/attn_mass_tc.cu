@@ -49,7 +49,6 @@ namespace {
 
 constexpr int BM = 128;            // rows of the fixed A tile (TMEM lanes)
 constexpr int BN = 128;            // rows of a streamed B tile (TMEM columns per accumulator)
-constexpr int HD = 128;            // head dim (MMA K)
 constexpr int NSTAGE = 2;          // B tiles in flight
 constexpr int NACC = 2;            // TMEM accumulators
 
@@ -65,29 +64,33 @@ struct Epi {
   static constexpr int MMA = WARPS + 1;
   static constexpr int THREADS = 32 * (WARPS + 2);
 };
-constexpr int TILE_BYTES = 128 * HD * 2;         // 32 KB: two 128-row x 128-byte halves
-constexpr int HALF_BYTES = TILE_BYTES / 2;
 constexpr int TMEM_COLS = NACC * BN;             // 256
 
 constexpr int EXT_K = 16;                        // extra MMA K-step of the mass pass
 constexpr int EXT_BYTES = 128 * EXT_K * 2;       // one [128 x 16] 16-bit operand (4 KB)
 
-constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + TILE_BYTES;
-constexpr int OFF_BAR = OFF_B + NSTAGE * TILE_BYTES;
-constexpr int OFF_MISC = OFF_BAR + 256;
-constexpr int OFF_AEXT = OFF_MISC + 256;         // key-side extension: [1, 1, 1, 0, ...] per row
-constexpr int OFF_BEXT = OFF_AEXT + EXT_BYTES;   // query-side extension per stage: -lse/scale split
-constexpr int OFF_RED = OFF_BEXT + NSTAGE * EXT_BYTES;
+// Shared-memory layout for head dim HD (the MMA K): a 128-row tile is HD/64 TMA boxes of
+// 128 rows x 128 bytes (16 KB each, 128-byte swizzle).
+template <int HD>
+struct Smem {
+  static_assert(HD == 64 || HD == 128, "head_dim 64 or 128");
+  static constexpr int HALVES = HD / 64;
+  static constexpr int HALF_BYTES = 128 * 64 * 2;
+  static constexpr int TILE_BYTES = HALVES * HALF_BYTES;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_B + NSTAGE * TILE_BYTES;
+  static constexpr int OFF_MISC = OFF_BAR + 256;
+  static constexpr int OFF_AEXT = OFF_MISC + 256;          // key-side extension: [1, 1, 1, 0, ...]
+  static constexpr int OFF_BEXT = OFF_AEXT + EXT_BYTES;    // query-side extension per stage
+  static constexpr int OFF_RED = OFF_BEXT + NSTAGE * EXT_BYTES;
+  static constexpr int OFF_RANK = OFF_AEXT;                // sparse LSE: rank ring (no extension)
+  // row-state exchange of the epilogue (NCG - 1 groups of [m | l] per row) + alignment slack
+  static constexpr int BYTES = OFF_RED + (Epi<0>::NCG - 1) * 2 * BM * 4 + 1024;
+};
 // Sparse LSE pass: ranks of the last NRK key tiles (the extension operands are unused there).
 constexpr int NRK = 8;
-constexpr int OFF_RANK = OFF_AEXT;
-static_assert(NRK * BN * 4 <= OFF_RED - OFF_AEXT, "rank ring must fit in the extension area");
-// Row-state exchange of the epilogue (NCG - 1 groups of [m | l] per row).
-template <int MODE>
-__host__ __device__ constexpr int off_red() { return OFF_RED; }
-template <int MODE>
-constexpr int smem_bytes() { return off_red<MODE>() + (Epi<MODE>::NCG - 1) * 2 * BM * 4 + 1024; }   // + alignment slack
+static_assert(NRK * BN * 4 <= Smem<128>::OFF_RED - Smem<128>::OFF_AEXT, "rank ring must fit in the extension area");
 
 // Byte offset of element (r, k) of a [128 x 16] K-major operand in 8 x 16-byte core matrices
 // (core (r/8, k/8) at (r/8)*256 + (k/8)*128): the layout desc_noswz(addr, 128, 256) reads.
@@ -212,29 +215,31 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return d;
 }
 
-template <int MODE>
+template <int MODE, int HD>
 __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmE, const TcParams p, const bool bf16) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = ptx::smem_u32(smem);
-  const uint32_t sA = s_base + OFF_A;
-  const uint32_t sB = s_base + OFF_B;
-  const uint32_t bar_full = s_base + OFF_BAR;                  // [NSTAGE]
+  using L = Smem<HD>;
+  constexpr int TILE_BYTES = L::TILE_BYTES, HALF_BYTES = L::HALF_BYTES;
+  const uint32_t sA = s_base + L::OFF_A;
+  const uint32_t sB = s_base + L::OFF_B;
+  const uint32_t bar_full = s_base + L::OFF_BAR;                  // [NSTAGE]
   const uint32_t bar_empty = bar_full + 8 * NSTAGE;            // [NSTAGE]
   const uint32_t bar_accf = bar_empty + 8 * NSTAGE;            // [NACC]
   const uint32_t bar_acce = bar_accf + 8 * NACC;               // [NACC]
   const uint32_t bar_a = bar_acce + 8 * NACC;
   const uint32_t bar_rk = bar_a + 8;                           // [NRK] sparse LSE: ranks staged
-  int* rbuf = reinterpret_cast<int*>(smem + OFF_RANK);         // [NRK][BN]
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
-  float* red = reinterpret_cast<float*>(smem + off_red<MODE>());
+  int* rbuf = reinterpret_cast<int*>(smem + L::OFF_RANK);         // [NRK][BN]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+  float* red = reinterpret_cast<float*>(smem + L::OFF_RED);
   constexpr int EPI_WARPS = Epi<MODE>::WARPS, PRODUCER_WARP = Epi<MODE>::PRODUCER, MMA_WARP = Epi<MODE>::MMA;
   constexpr int NCG = Epi<MODE>::NCG, CW = Epi<MODE>::CW;
-  const uint32_t sAext = s_base + OFF_AEXT;
-  const uint32_t sBext = s_base + OFF_BEXT;
+  const uint32_t sAext = s_base + L::OFF_AEXT;
+  const uint32_t sBext = s_base + L::OFF_BEXT;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   Item it = decode_item<MODE>(blockIdx.x, p);
@@ -262,7 +267,7 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
     ptx::prefetch_tmap(&tmQ);
     ptx::prefetch_tmap(&tmK);
   }
-  int* tau_red = reinterpret_cast<int*>(smem + OFF_MISC + 16);      // sparse pass: [4] max, [4] min
+  int* tau_red = reinterpret_cast<int*>(smem + L::OFF_MISC + 16);      // sparse pass: [4] max, [4] min
   if (MODE == 2 && p.inv != nullptr && warp < 4) {
     // cutoff range over the query tile's rows (rows past S ignored)
     const int kvz = (it.group / p.Hq) * p.Hkv + (it.group % p.Hq) / p.G;
@@ -281,13 +286,13 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
     const uint16_t one = bf16 ? 0x3F80u : 0x3C00u;
     for (int e = threadIdx.x; e < 128 * EXT_K; e += EPI_WARPS * 32) {
       const int r = e / EXT_K, k = e % EXT_K;
-      *reinterpret_cast<uint16_t*>(smem + OFF_AEXT + ext_off(r, k)) = k < 3 ? one : 0u;
+      *reinterpret_cast<uint16_t*>(smem + L::OFF_AEXT + ext_off(r, k)) = k < 3 ? one : 0u;
     }
     // B side, per stage: rows 0..127 of k = 0..7 (written by TMA from the prepared array) at
     // 16-byte row pitch, then the k = 8..15 half, which stays zero.
     for (int e = threadIdx.x; e < NSTAGE * EXT_BYTES / 16; e += EPI_WARPS * 32) {
       const int st = e / (EXT_BYTES / 16), off = (e % (EXT_BYTES / 16)) * 16;
-      if (off >= EXT_BYTES / 2) *reinterpret_cast<uint4*>(smem + OFF_BEXT + st * EXT_BYTES + off) = make_uint4(0u, 0u, 0u, 0u);
+      if (off >= EXT_BYTES / 2) *reinterpret_cast<uint4*>(smem + L::OFF_BEXT + st * EXT_BYTES + off) = make_uint4(0u, 0u, 0u, 0u);
     }
     ptx::fence_proxy_async_smem();
   }
@@ -296,18 +301,20 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  // Coordinates of the fixed A tile and of streamed tile t.
-  int a_row, a_z, kv_z = 0, b_of_group = 0, hkv = 0;
+  // Coordinates of the fixed A tile and of streamed tile t.  Q and K tensor maps are 4-D
+  // (feature, token, head, batch); the A tile is (a_row, a_h, b_of_group).
+  int a_row, a_h, kv_z = 0, b_of_group = 0, hkv = 0;
   if (MODE != 1) {
     a_row = it.tile * BM;
-    a_z = it.group;
     b_of_group = it.group / p.Hq;
-    kv_z = b_of_group * p.Hkv + (it.group % p.Hq) / p.G;
+    a_h = it.group % p.Hq;                    // query head
+    hkv = a_h / p.G;
+    kv_z = b_of_group * p.Hkv + hkv;
   } else {
     a_row = it.tile * BM;
-    a_z = it.group;                // K tensor map z = b*Hkv + h
     b_of_group = it.group / p.Hkv;
     hkv = it.group % p.Hkv;
+    a_h = hkv;                                // KV head
   }
   // Sparse pass, rank-ordered plan of a query tile whose rows all have a cutoff: the key tiles
   // holding the sinks and the protected windows in position order (eligible keys there are
@@ -343,14 +350,15 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
   const int j0 = it.tile * BM;     // mass pass: first key of the tile
   // mass pass: streamed tile t is query tile u of query head gh of the group (t = gh * per_head + u;
   // both loops below keep (gh, u) as running counters instead of dividing)
-  auto b_coords = [&](int t, int gh, int u, int& row, int& z) {
+  // (row, head) of streamed tile t in its tensor map (the batch is b_of_group)
+  auto b_coords = [&](int t, int gh, int u, int& row, int& h) {
     if (MODE != 1) {
       const int kt = key_tile(t);
       row = kt >= 0 ? kt * BN : (t - n_pos) * BN;
-      z = kv_z;
+      h = hkv;
     } else {
       row = j0 + p.window + BN * (it.chunk * p.TPC + u);
-      z = b_of_group * p.Hq + hkv * p.G + gh;
+      h = hkv * p.G + gh;
     }
   };
 
@@ -359,8 +367,9 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
     const CUtensorMap* tmB = MODE != 1 ? &tmK : &tmQ;
     if (lane == 0) {
       ptx::mbar_arrive_expect_tx(bar_a, TILE_BYTES);
-      ptx::tma_load_3d(sA, tmA, bar_a, 0, a_row, a_z);
-      ptx::tma_load_3d(sA + HALF_BYTES, tmA, bar_a, 64, a_row, a_z);
+#pragma unroll
+      for (int hb = 0; hb < L::HALVES; ++hb)
+        ptx::tma_load_4d(sA + hb * HALF_BYTES, tmA, bar_a, 64 * hb, a_row, a_h, b_of_group);
     }
     if (lane == 0) ptx::prefetch_tmap(&tmE);
     int t = 0, pgh = 0, pu = 0;
@@ -375,17 +384,19 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
       if (use > 0) ok = ptx::mbar_wait(bar_empty + 8 * s, (use - 1) & 1, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, ok)) break;
       if (lane == 0) {
-        int row, z;
-        b_coords(t, gh, u, row, z);
+        int row, h;
+        b_coords(t, gh, u, row, h);
         const uint32_t dst = sB + s * TILE_BYTES;
         // Mass pass: the stage also receives the 128 query rows' -lse/scale extension (three
         // 16-bit parts per row, prepared in global memory) by its own TMA box.
         ptx::mbar_arrive_expect_tx(bar_full + 8 * s, TILE_BYTES + (MODE == 1 ? EXT_BYTES / 2 : 0));
         // sparse pass, rank-ordered tiles: the keys in rank order (third tensor map)
         const CUtensorMap* src = (MODE == 2 && rank_mode && key_tile(t) < 0) ? &tmE : tmB;
-        ptx::tma_load_3d(dst, src, bar_full + 8 * s, 0, row, z);
-        ptx::tma_load_3d(dst + HALF_BYTES, src, bar_full + 8 * s, 64, row, z);
-        if (MODE == 1) ptx::tma_load_3d(sBext + s * EXT_BYTES, &tmE, bar_full + 8 * s, 0, row, z);
+#pragma unroll
+        for (int hb = 0; hb < L::HALVES; ++hb)
+          ptx::tma_load_4d(dst + hb * HALF_BYTES, src, bar_full + 8 * s, 64 * hb, row, h, b_of_group);
+        if (MODE == 1)
+          ptx::tma_load_3d(sBext + s * EXT_BYTES, &tmE, bar_full + 8 * s, 0, row, b_of_group * p.Hq + h);
       }
       if (MODE == 2) {
         // Per-column data of the tile for the epilogue's mask: the ranks of a position-ordered
@@ -706,26 +717,28 @@ __global__ void ext_prep_kernel(const float* __restrict__ lse, int BHq, int S, i
 }
 
 // Sparse pass, rank-ordered stream, in one scatter over the keys: inv[h, rank[h, j]] = j and
-// ks[h, rank[h, j]] = k[h, j].  inv starts at -1; a rank outside [0, S) or a rank met twice (the
-// previous inv entry was already set) clears *ok.  S in-range ranks without a repeat are a
-// permutation, so *ok stays nonzero exactly when ks and inv are complete.
-constexpr int RS_VPR = HD * 2 / 16;        // 16-byte vectors per key row
-
-__global__ void rank_scatter_keys_kernel(const uint4* __restrict__ k, const int32_t* __restrict__ ranks,
-                                         int S, long long total, int32_t* __restrict__ inv,
+// ks[h, rank[h, j]] = k[h, j] (ks dense [B*Hkv, S, D]; k read through its element strides).
+// inv starts at -1; a rank outside [0, S) or a rank met twice (the previous inv entry was already
+// set) clears *ok.  S in-range ranks without a repeat are a permutation, so *ok stays nonzero
+// exactly when ks and inv are complete.
+__global__ void rank_scatter_keys_kernel(const uint16_t* __restrict__ k, long long k_sb, long long k_sh,
+                                         long long k_sr, int Hkv, const int32_t* __restrict__ ranks,
+                                         int S, int vpr, long long total, int32_t* __restrict__ inv,
                                          uint4* __restrict__ ks, int* ok) {
   for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
        e += (long long)gridDim.x * blockDim.x) {
-    const long long hj = e / RS_VPR;                 // h * S + j
-    const int c = (int)(e - hj * RS_VPR);
+    const long long hj = e / vpr;                    // h * S + j, h = b * Hkv + hk
+    const int c = (int)(e - hj * vpr);
     const long long h = hj / S;
+    const int j = (int)(hj - h * S);
     const int r = ranks[hj];
     if ((unsigned)r >= (unsigned)S) {
       if (c == 0) *ok = 0;
       continue;
     }
-    if (c == 0 && atomicExch(inv + h * S + r, (int)(hj - h * S)) != -1) *ok = 0;
-    ks[(h * S + r) * RS_VPR + c] = k[e];
+    if (c == 0 && atomicExch(inv + h * S + r, j) != -1) *ok = 0;
+    const uint16_t* src = k + (h / Hkv) * k_sb + (h % Hkv) * k_sh + (long long)j * k_sr;
+    ks[(h * S + r) * vpr + c] = reinterpret_cast<const uint4*>(src)[c];
   }
 }
 
@@ -782,19 +795,30 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [n_heads, S, 128] tensor, 128-row x 64-element boxes, 128-byte swizzle, zero fill past S.
-bool make_tmap(CUtensorMap* m, const void* base, int dtype, int n_heads, int S) {
+// [n_batch, n_heads, S, D] tensor with element strides (sb, sh, sr) (D contiguous) as a 4-D map
+// (feature, token, head, batch): 128-row x 64-element boxes, 128-byte swizzle, zero fill past S.
+// The stride of a dimension of extent 1 is never applied; it is replaced by a valid value.
+bool make_tmap(CUtensorMap* m, const void* base, int dtype, int D, int S, int n_heads, int n_batch,
+               long long sr, long long sh, long long sb) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)HD, (cuuint64_t)S, (cuuint64_t)n_heads};
-  cuuint64_t strides[2] = {(cuuint64_t)HD * 2, (cuuint64_t)S * HD * 2};
-  cuuint32_t box[3] = {64, 128, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
+  if (n_heads == 1) sh = sr * S;
+  if (n_batch == 1) sb = sh * n_heads;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)n_heads, (cuuint64_t)n_batch};
+  cuuint64_t strides[3] = {(cuuint64_t)sr * 2, (cuuint64_t)sh * 2, (cuuint64_t)sb * 2};
+  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapDataType dt =
       dtype == KVP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+  return enc(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+bool make_q_tmap(CUtensorMap* m, const void* q, int dtype, const AttnShape& s) {
+  return make_tmap(m, q, dtype, s.head_dim, s.seq_len, s.h_q, s.n_batch, s.q_sr, s.q_sh, s.q_sb);
+}
+bool make_k_tmap(CUtensorMap* m, const void* k, int dtype, const AttnShape& s) {
+  return make_tmap(m, k, dtype, s.head_dim, s.seq_len, s.h_kv, s.n_batch, s.k_sr, s.k_sh, s.k_sb);
 }
 
 // Tensor map of the mass pass's query-side extension [n_heads, S_pad, 8] (16-byte rows, boxes of
@@ -840,27 +864,32 @@ FamSched fam_schedule(AttnShape s, int window) {
   return f;
 }
 
-template <int MODE>
-cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& te, const TcParams& p,
-                      int grid, bool bf16, cudaStream_t st) {
-  auto kern = attn_tc_kernel<MODE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<MODE>());
+template <int MODE, int HD>
+cudaError_t launch_tc_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& te, const TcParams& p,
+                         int grid, bool bf16, cudaStream_t st) {
+  auto kern = attn_tc_kernel<MODE, HD>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<HD>::BYTES);
   if (e != cudaSuccess) return e;
   count_launches(1);
-  kern<<<grid, Epi<MODE>::THREADS, smem_bytes<MODE>(), st>>>(tq, tk, te, p, bf16);
+  kern<<<grid, Epi<MODE>::THREADS, Smem<HD>::BYTES, st>>>(tq, tk, te, p, bf16);
   return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& te, const TcParams& p,
+                      int grid, bool bf16, int head_dim, cudaStream_t st) {
+  return head_dim == 64 ? launch_tc_hd<MODE, 64>(tq, tk, te, p, grid, bf16, st)
+                        : launch_tc_hd<MODE, 128>(tq, tk, te, p, grid, bf16, st);
 }
 
 }  // namespace
 
-size_t sparse_lse_workspace_size(int dtype, AttnShape s) {
-  if (!tc_supported(dtype, s)) return 0;
-  const size_t n = (size_t)s.n_batch * s.h_kv * s.seq_len;
-  return ((n * 4 + 255) & ~(size_t)255) + ((n * HD * 2 + 255) & ~(size_t)255) + 256;
-}
+bool tc_encoder_available() { return encode_fn() != nullptr; }
 
-bool tc_supported(int dtype, AttnShape s) {
-  return (dtype == KVP_BF16 || dtype == KVP_F16) && s.head_dim == HD && encode_fn() != nullptr;
+size_t sparse_lse_workspace_size(int dtype, AttnShape s) {
+  if (dtype != KVP_BF16 && dtype != KVP_F16) return 0;
+  const size_t n = (size_t)s.n_batch * s.h_kv * s.seq_len;
+  return ((n * 4 + 255) & ~(size_t)255) + ((n * s.head_dim * 2 + 255) & ~(size_t)255) + 256;
 }
 
 // Workspace of the mass pass: partial sums, then the query-side extension (16 bytes per query
@@ -878,9 +907,7 @@ size_t fam_tc_workspace_size(AttnShape s, int window, int per_head) {
 cudaError_t launch_lse_tc(const void* q, const void* k, int dtype, AttnShape s, float scale,
                           float* lse, int* status, cudaStream_t st, const SparseMask* mask) {
   CUtensorMap tq, tk;
-  if (!make_tmap(&tq, q, dtype, s.n_batch * s.h_q, s.seq_len) ||
-      !make_tmap(&tk, k, dtype, s.n_batch * s.h_kv, s.seq_len))
-    return cudaErrorInvalidValue;
+  if (!make_q_tmap(&tq, q, dtype, s) || !make_k_tmap(&tk, k, dtype, s)) return cudaErrorInvalidValue;
   TcParams p{};
   p.S = s.seq_len;
   p.Hq = s.h_q;
@@ -891,13 +918,14 @@ cudaError_t launch_lse_tc(const void* q, const void* k, int dtype, AttnShape s, 
   p.n_groups = s.n_batch * s.h_q;
   p.NQT = (s.seq_len + BM - 1) / BM;
   p.status = status;
+  const bool bf16 = dtype == KVP_BF16;
   if (mask) {
     p.ranks = mask->ranks;
     p.tau = mask->tau;
     p.n_sink = mask->n_sink;
     p.window = mask->window;
     p.ranks_vec = s.seq_len % 4 == 0 && ((uintptr_t)mask->ranks & 15) == 0;
-    if (!mask->inv) return launch_tc<2>(tq, tk, tk, p, p.n_groups * p.NQT, dtype == KVP_BF16, st);
+    if (!mask->inv) return launch_tc<2>(tq, tk, tk, p, p.n_groups * p.NQT, bf16, s.head_dim, st);
     // rank-ordered stream: inverse permutation, keys in rank order, validity flag
     const int BHkv = s.n_batch * s.h_kv;
     const long long n = (long long)BHkv * s.seq_len;
@@ -908,21 +936,26 @@ cudaError_t launch_lse_tc(const void* q, const void* k, int dtype, AttnShape s, 
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int vpr = s.head_dim * 2 / 16;
     const long long cap = (long long)sms * 8;
-    long long b2 = (n * RS_VPR + 255) / 256;
+    long long b2 = (n * vpr + 255) / 256;
     b2 = b2 > cap ? cap : b2;
     count_launches(1);
-    rank_scatter_keys_kernel<<<(unsigned)b2, 256, 0, st>>>((const uint4*)k, mask->ranks, s.seq_len, n * RS_VPR,
-                                                           mask->inv, (uint4*)mask->k_sorted, mask->perm_ok);
+    rank_scatter_keys_kernel<<<(unsigned)b2, 256, 0, st>>>((const uint16_t*)k, s.k_sb, s.k_sh, s.k_sr, s.h_kv,
+                                                           mask->ranks, s.seq_len, vpr, n * vpr, mask->inv,
+                                                           (uint4*)mask->k_sorted, mask->perm_ok);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     CUtensorMap tks;
-    if (!make_tmap(&tks, mask->k_sorted, dtype, BHkv, s.seq_len)) return cudaErrorInvalidValue;
+    const long long sd = (long long)s.seq_len * s.head_dim;
+    if (!make_tmap(&tks, mask->k_sorted, dtype, s.head_dim, s.seq_len, s.h_kv, s.n_batch, s.head_dim, sd,
+                   sd * s.h_kv))
+      return cudaErrorInvalidValue;
     p.inv = mask->inv;
     p.perm_ok = mask->perm_ok;
-    return launch_tc<2>(tq, tk, tks, p, p.n_groups * p.NQT, dtype == KVP_BF16, st);
+    return launch_tc<2>(tq, tk, tks, p, p.n_groups * p.NQT, bf16, s.head_dim, st);
   }
-  return launch_tc<0>(tq, tk, tk, p, p.n_groups * p.NQT, dtype == KVP_BF16, st);
+  return launch_tc<0>(tq, tk, tk, p, p.n_groups * p.NQT, bf16, s.head_dim, st);
 }
 
 cudaError_t launch_fam_tc(const void* q, const void* k, const float* lse, int dtype, AttnShape s,
@@ -953,8 +986,7 @@ cudaError_t launch_fam_tc(const void* q, const void* k, const float* lse, int dt
     const int BHq = s.n_batch * s.h_q, S_pad = s.seq_len + BN;
     void* ext = (char*)ws + fam_partial_bytes(s, f, per_head);
     CUtensorMap tq, tk, te;
-    if (!make_tmap(&tq, q, dtype, BHq, s.seq_len) ||
-        !make_tmap(&tk, k, dtype, s.n_batch * s.h_kv, s.seq_len) ||
+    if (!make_q_tmap(&tq, q, dtype, s) || !make_k_tmap(&tk, k, dtype, s) ||
         !make_ext_tmap(&te, ext, dtype, BHq, S_pad))
       return cudaErrorInvalidValue;
     if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
@@ -969,7 +1001,7 @@ cudaError_t launch_fam_tc(const void* q, const void* k, const float* lse, int dt
                                                      dtype == KVP_BF16, (uint4*)ext);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = launch_tc<1>(tq, tk, te, p, (int)items, dtype == KVP_BF16, st);
+    e = launch_tc<1>(tq, tk, te, p, (int)items, dtype == KVP_BF16, s.head_dim, st);
     if (e != cudaSuccess) return e;
   }
   count_launches(1);

@@ -34,6 +34,7 @@ static __device__ __align__(256) unsigned char g_decode_noalloc_scratch[KVP_DECO
 constexpr int kNoallocMaxDevices = 64;
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[kNoallocMaxDevices] = {nullptr};
+void* g_noalloc_ctx[kNoallocMaxDevices] = {nullptr};   // context each cached address belongs to
 
 constexpr int MAXG = 8;
 constexpr int DEC_WARPS = 4;
@@ -273,19 +274,31 @@ DecodePlan decode_plan(int n_layers, int h_q, int h_kv, int head_dim, int T_cap,
 
 // Device address of the static decode scratch on the current device.  In host
 // code the array's name only stands in for the symbol, so the address is
-// looked up with cudaGetSymbolAddress, once per device, with that device
-// current, and cached.
+// looked up with cudaGetSymbolAddress, with that device current, and cached
+// per device together with the CUDA context it belongs to: a new context on
+// the device (after cudaDeviceReset) loads the module again, possibly at
+// another address, and the address is then looked up again.
+bool decode_noalloc_scratch_ready() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoallocMaxDevices) return false;
+  void* ctx = current_cu_context();
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  return g_noalloc_ptr[dev] != nullptr && g_noalloc_ctx[dev] == ctx;
+}
+
 cudaError_t decode_noalloc_scratch(void** ptr, size_t* bytes) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kNoallocMaxDevices) return cudaErrorInvalidDevice;
+  void* ctx = current_cu_context();
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  if (!g_noalloc_ptr[dev] || g_noalloc_ctx[dev] != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_decode_noalloc_scratch);
     if (e != cudaSuccess) return e;
     g_noalloc_ptr[dev] = p;
+    g_noalloc_ctx[dev] = ctx;
   }
   *ptr = g_noalloc_ptr[dev];
   *bytes = sizeof(g_decode_noalloc_scratch);

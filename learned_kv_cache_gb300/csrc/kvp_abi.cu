@@ -28,6 +28,7 @@ __device__ int g_device_status;
 constexpr int kMaxDevices = 64;
 std::mutex g_status_mu;
 int* g_status_ptr[kMaxDevices] = {nullptr};
+void* g_status_ctx[kMaxDevices] = {nullptr};   // context each cached address belongs to
 
 int fail(int code, const char* fmt, ...) {
   char buf[512];
@@ -43,18 +44,20 @@ int cuda_fail(cudaError_t e, const char* where) {
   return fail(KVP_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
-// Device address of this device's status word (looked up once per device).
+// Device address of this device's status word (looked up once per device and context).
 int status_ptr(int** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return fail(KVP_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  void* ctx = kvp::current_cu_context();
   std::lock_guard<std::mutex> lock(g_status_mu);
-  if (!g_status_ptr[dev]) {
+  if (!g_status_ptr[dev] || g_status_ctx[dev] != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_device_status);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
     g_status_ptr[dev] = (int*)p;
+    g_status_ctx[dev] = ctx;
   }
   *out = g_status_ptr[dev];
   return KVP_OK;
@@ -81,6 +84,49 @@ int check_attn_shape(int n_batch, int h_q, int h_kv, int S, int D) {
   return KVP_OK;
 }
 
+// Shape and Q/K element strides of an attention pass.  strides == NULL means dense
+// [n_batch, H, S, D]; otherwise {batch, head, token} strides in elements, each a positive
+// multiple of 16 bytes (the head_dim axis is contiguous).  Strides of extent-1 dimensions are
+// not used.
+int attn_shape(int dtype, int n_batch, int h_q, int h_kv, int S, int D, const int64_t* q_strides,
+               const int64_t* k_strides, kvp::AttnShape* out) {
+  kvp::AttnShape s = kvp::dense_attn_shape(n_batch, h_q, h_kv, S, D);
+  const int elt = elem_size(dtype);
+  const int64_t* src[2] = {q_strides, k_strides};
+  int64_t* dst[2] = {&s.q_sb, &s.k_sb};
+  const char* name[2] = {"q_strides", "k_strides"};
+  for (int t = 0; t < 2; ++t) {
+    if (!src[t]) continue;
+    for (int i = 0; i < 3; ++i) {
+      const int64_t v = src[t][i];
+      const bool used = i == 2 || (i == 0 ? n_batch > 1 : (t == 0 ? h_q : h_kv) > 1);
+      if (!used) continue;
+      if (v <= 0 || (v * elt) % 16 != 0 || v * elt >= (1LL << 40))
+        return fail(KVP_ERR_INVALID_ARG,
+                    "%s[%d]=%lld: strides must be positive multiples of 16 bytes below 2^40 bytes",
+                    name[t], i, (long long)v);
+      if (i == 2 && v < D)
+        return fail(KVP_ERR_INVALID_ARG, "%s token stride %lld < head_dim %d", name[t], (long long)v, D);
+    }
+    dst[t][0] = n_batch > 1 ? src[t][0] : dst[t][0];
+    dst[t][1] = (t == 0 ? h_q : h_kv) > 1 ? src[t][1] : dst[t][1];
+    dst[t][2] = src[t][2];
+  }
+  *out = s;
+  return KVP_OK;
+}
+
+// bf16 / f16 inputs run on the tensor-core passes, float32 inputs on the fp32-FFMA passes; there
+// is no other path.  The tensor-core passes need the driver's tensor-map encoder.
+int use_tensor_cores(int dtype, bool* tc) {
+  *tc = dtype != KVP_F32;
+  if (*tc && !kvp::tc_encoder_available())
+    return fail(KVP_ERR_CUDA,
+                "cuTensorMapEncodeTiled could not be resolved from the CUDA driver; bf16/f16 inputs "
+                "run only on the tensor-core (TMA) passes");
+  return KVP_OK;
+}
+
 std::atomic<unsigned long long> g_launches{0};
 
 #define KVP_TRY(x)            \
@@ -93,6 +139,22 @@ std::atomic<unsigned long long> g_launches{0};
 
 namespace kvp {
 void count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+
+void* current_cu_context() {
+  typedef int (*CtxGetCurrentFn)(void**);
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  void* ctx = nullptr;
+  if (fn && fn(&ctx) != 0) ctx = nullptr;
+  return ctx;
+}
 }  // namespace kvp
 
 extern "C" {
@@ -132,19 +194,22 @@ int kvp_check_device_status(kvp_stream_t stream) {
 }
 
 int kvp_lse_pass(const void* q, const void* k, int dtype, int n_batch, int h_q, int h_kv,
-                 int seq_len, int head_dim, float sm_scale, float* lse, kvp_stream_t stream) {
+                 int seq_len, int head_dim, const int64_t* q_strides, const int64_t* k_strides,
+                 float sm_scale, float* lse, kvp_stream_t stream) {
   g_last_error.clear();
   KVP_TRY(check_dtype(dtype));
   KVP_TRY(check_attn_shape(n_batch, h_q, h_kv, seq_len, head_dim));
   if (!q || !k || !lse) return fail(KVP_ERR_INVALID_ARG, "null q/k/lse");
   if (!aligned16(q) || !aligned16(k)) return fail(KVP_ERR_INVALID_ARG, "q/k not 16-byte aligned");
   if (!std::isfinite(sm_scale)) return fail(KVP_ERR_INVALID_ARG, "sm_scale not finite");
+  kvp::AttnShape s;
+  KVP_TRY(attn_shape(dtype, n_batch, h_q, h_kv, seq_len, head_dim, q_strides, k_strides, &s));
+  bool tc = false;
+  KVP_TRY(use_tensor_cores(dtype, &tc));
   int* st = nullptr;
   KVP_TRY(status_ptr(&st));
-  kvp::AttnShape s{n_batch, h_q, h_kv, seq_len, head_dim};
-  cudaError_t e = kvp::tc_supported(dtype, s)
-                      ? kvp::launch_lse_tc(q, k, dtype, s, sm_scale, lse, st, (cudaStream_t)stream)
-                      : kvp::launch_lse_simt(q, k, dtype, s, sm_scale, lse, (cudaStream_t)stream);
+  cudaError_t e = tc ? kvp::launch_lse_tc(q, k, dtype, s, sm_scale, lse, st, (cudaStream_t)stream)
+                     : kvp::launch_lse_simt(q, k, dtype, s, sm_scale, lse, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "kvp_lse_pass launch");
   return KVP_OK;
 }
@@ -168,13 +233,14 @@ int kvp_topk_cutoffs(const int32_t* ranks, int n_heads, int seq_len, int n_sink,
 size_t kvp_sparse_lse_workspace_size(int dtype, int n_batch, int h_q, int h_kv, int seq_len, int head_dim) {
   if (check_dtype(dtype) != KVP_OK || check_attn_shape(n_batch, h_q, h_kv, seq_len, head_dim) != KVP_OK)
     return 0;
-  return kvp::sparse_lse_workspace_size(dtype, kvp::AttnShape{n_batch, h_q, h_kv, seq_len, head_dim});
+  return kvp::sparse_lse_workspace_size(dtype, kvp::dense_attn_shape(n_batch, h_q, h_kv, seq_len, head_dim));
 }
 
 int kvp_sparse_lse_pass(const void* q, const void* k, const int32_t* ranks, const int32_t* tau,
                         int dtype, int n_batch, int h_q, int h_kv, int seq_len, int head_dim,
-                        float sm_scale, int n_sink, int window, float* lse, void* workspace,
-                        size_t workspace_bytes, kvp_stream_t stream) {
+                        const int64_t* q_strides, const int64_t* k_strides, float sm_scale,
+                        int n_sink, int window, float* lse, void* workspace, size_t workspace_bytes,
+                        kvp_stream_t stream) {
   g_last_error.clear();
   KVP_TRY(check_dtype(dtype));
   KVP_TRY(check_attn_shape(n_batch, h_q, h_kv, seq_len, head_dim));
@@ -182,9 +248,12 @@ int kvp_sparse_lse_pass(const void* q, const void* k, const int32_t* ranks, cons
   if (!aligned16(q) || !aligned16(k)) return fail(KVP_ERR_INVALID_ARG, "q/k not 16-byte aligned");
   if (!std::isfinite(sm_scale)) return fail(KVP_ERR_INVALID_ARG, "sm_scale not finite");
   if (n_sink < 0 || window < 0) return fail(KVP_ERR_INVALID_ARG, "n_sink=%d window=%d", n_sink, window);
+  kvp::AttnShape s;
+  KVP_TRY(attn_shape(dtype, n_batch, h_q, h_kv, seq_len, head_dim, q_strides, k_strides, &s));
+  bool tc = false;
+  KVP_TRY(use_tensor_cores(dtype, &tc));
   int* st = nullptr;
   KVP_TRY(status_ptr(&st));
-  kvp::AttnShape s{n_batch, h_q, h_kv, seq_len, head_dim};
   kvp::SparseMask mask{ranks, tau, n_sink, window};
   const size_t need = kvp::sparse_lse_workspace_size(dtype, s);
   if (need > 0) {
@@ -192,14 +261,15 @@ int kvp_sparse_lse_pass(const void* q, const void* k, const int32_t* ranks, cons
       return fail(KVP_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
     if (((uintptr_t)workspace & 255) != 0) return fail(KVP_ERR_INVALID_ARG, "workspace not 256-byte aligned");
     const size_t n = (size_t)n_batch * h_kv * seq_len;
+    const size_t inv_bytes = (n * 4 + 255) & ~(size_t)255;
+    const size_t ks_bytes = (n * (size_t)head_dim * 2 + 255) & ~(size_t)255;
     char* w = (char*)workspace;
     mask.inv = (int32_t*)w;
-    mask.k_sorted = w + ((n * 4 + 255) & ~(size_t)255);
-    mask.perm_ok = (int*)(w + ((n * 4 + 255) & ~(size_t)255) + ((n * 128 * 2 + 255) & ~(size_t)255));
+    mask.k_sorted = w + inv_bytes;
+    mask.perm_ok = (int*)(w + inv_bytes + ks_bytes);
   }
-  cudaError_t e = kvp::tc_supported(dtype, s)
-                      ? kvp::launch_lse_tc(q, k, dtype, s, sm_scale, lse, st, (cudaStream_t)stream, &mask)
-                      : kvp::launch_lse_simt(q, k, dtype, s, sm_scale, lse, (cudaStream_t)stream, &mask);
+  cudaError_t e = tc ? kvp::launch_lse_tc(q, k, dtype, s, sm_scale, lse, st, (cudaStream_t)stream, &mask)
+                     : kvp::launch_lse_simt(q, k, dtype, s, sm_scale, lse, (cudaStream_t)stream, &mask);
   if (e != cudaSuccess) return cuda_fail(e, "kvp_sparse_lse_pass launch");
   return KVP_OK;
 }
@@ -209,13 +279,14 @@ size_t kvp_future_attn_mass_workspace_size(int dtype, int n_batch, int h_q, int 
   if (check_dtype(dtype) != KVP_OK || check_attn_shape(n_batch, h_q, h_kv, seq_len, head_dim) != KVP_OK ||
       window < 0)
     return 0;
-  kvp::AttnShape s{n_batch, h_q, h_kv, seq_len, head_dim};
-  return kvp::tc_supported(dtype, s) ? kvp::fam_tc_workspace_size(s, window) : 0;
+  const kvp::AttnShape s = kvp::dense_attn_shape(n_batch, h_q, h_kv, seq_len, head_dim);
+  return dtype != KVP_F32 ? kvp::fam_tc_workspace_size(s, window) : 0;
 }
 
 int kvp_future_attn_mass(const void* q, const void* k, const float* lse, int dtype, int n_batch,
-                         int h_q, int h_kv, int seq_len, int head_dim, float sm_scale, int window,
-                         float* F, void* workspace, size_t workspace_bytes, kvp_stream_t stream) {
+                         int h_q, int h_kv, int seq_len, int head_dim, const int64_t* q_strides,
+                         const int64_t* k_strides, float sm_scale, int window, float* F,
+                         void* workspace, size_t workspace_bytes, kvp_stream_t stream) {
   g_last_error.clear();
   KVP_TRY(check_dtype(dtype));
   KVP_TRY(check_attn_shape(n_batch, h_q, h_kv, seq_len, head_dim));
@@ -223,18 +294,19 @@ int kvp_future_attn_mass(const void* q, const void* k, const float* lse, int dty
   if (!aligned16(q) || !aligned16(k)) return fail(KVP_ERR_INVALID_ARG, "q/k not 16-byte aligned");
   if (window < 0) return fail(KVP_ERR_INVALID_ARG, "window=%d < 0", window);
   if (!std::isfinite(sm_scale)) return fail(KVP_ERR_INVALID_ARG, "sm_scale not finite");
-  kvp::AttnShape s{n_batch, h_q, h_kv, seq_len, head_dim};
+  kvp::AttnShape s;
+  KVP_TRY(attn_shape(dtype, n_batch, h_q, h_kv, seq_len, head_dim, q_strides, k_strides, &s));
+  bool tc = false;
+  KVP_TRY(use_tensor_cores(dtype, &tc));
   const size_t need = kvp_future_attn_mass_workspace_size(dtype, n_batch, h_q, h_kv, seq_len,
                                                           head_dim, window);
   if (need > 0 && (!workspace || workspace_bytes < need))
     return fail(KVP_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
   int* st = nullptr;
   KVP_TRY(status_ptr(&st));
-  cudaError_t e = kvp::tc_supported(dtype, s)
-                      ? kvp::launch_fam_tc(q, k, lse, dtype, s, sm_scale, window, F, workspace,
-                                           workspace_bytes, st, (cudaStream_t)stream)
-                      : kvp::launch_fam_simt(q, k, lse, dtype, s, sm_scale, window, F,
-                                             (cudaStream_t)stream);
+  cudaError_t e = tc ? kvp::launch_fam_tc(q, k, lse, dtype, s, sm_scale, window, F, workspace,
+                                          workspace_bytes, st, (cudaStream_t)stream)
+                     : kvp::launch_fam_simt(q, k, lse, dtype, s, sm_scale, window, F, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "kvp_future_attn_mass launch");
   return KVP_OK;
 }
@@ -248,15 +320,16 @@ size_t kvp_future_attn_target_workspace_size(int dtype, int n_batch, int h_q, in
   if (check_dtype(dtype) != KVP_OK || check_attn_shape(n_batch, h_q, h_kv, seq_len, head_dim) != KVP_OK ||
       window < 0)
     return 0;
-  kvp::AttnShape s{n_batch, h_q, h_kv, seq_len, head_dim};
-  const size_t part = kvp::tc_supported(dtype, s) ? kvp::fam_tc_workspace_size(s, window, 1) : 0;
+  const kvp::AttnShape s = kvp::dense_attn_shape(n_batch, h_q, h_kv, seq_len, head_dim);
+  const size_t part = dtype != KVP_F32 ? kvp::fam_tc_workspace_size(s, window, 1) : 0;
   return target_heads_bytes(n_batch, h_q, seq_len) + part;
 }
 
 int kvp_future_attn_target(const void* q, const void* k, const float* lse, int dtype, int n_batch,
-                           int h_q, int h_kv, int seq_len, int head_dim, float sm_scale, int window,
-                           float eps, int aggregate, float* target, float* F_heads, float* F,
-                           void* workspace, size_t workspace_bytes, kvp_stream_t stream) {
+                           int h_q, int h_kv, int seq_len, int head_dim, const int64_t* q_strides,
+                           const int64_t* k_strides, float sm_scale, int window, float eps,
+                           int aggregate, float* target, float* F_heads, float* F, void* workspace,
+                           size_t workspace_bytes, kvp_stream_t stream) {
   g_last_error.clear();
   KVP_TRY(check_dtype(dtype));
   KVP_TRY(check_attn_shape(n_batch, h_q, h_kv, seq_len, head_dim));
@@ -268,21 +341,23 @@ int kvp_future_attn_target(const void* q, const void* k, const float* lse, int d
   if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(KVP_ERR_INVALID_ARG, "eps must be finite and >= 0");
   if (aggregate != KVP_TARGET_MAX_LOG && aggregate != KVP_TARGET_MEAN_PROB)
     return fail(KVP_ERR_INVALID_ARG, "aggregate=%d", aggregate);
+  kvp::AttnShape s;
+  KVP_TRY(attn_shape(dtype, n_batch, h_q, h_kv, seq_len, head_dim, q_strides, k_strides, &s));
+  bool tc = false;
+  KVP_TRY(use_tensor_cores(dtype, &tc));
   const size_t need = kvp_future_attn_target_workspace_size(dtype, n_batch, h_q, h_kv, seq_len, head_dim, window);
   if (!workspace || workspace_bytes < need)
     return fail(KVP_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
   if (((uintptr_t)workspace & 255u) != 0) return fail(KVP_ERR_INVALID_ARG, "workspace not 256-byte aligned");
   int* st = nullptr;
   KVP_TRY(status_ptr(&st));
-  kvp::AttnShape s{n_batch, h_q, h_kv, seq_len, head_dim};
   float* heads = F_heads ? F_heads : (float*)workspace;
   char* part = (char*)workspace + target_heads_bytes(n_batch, h_q, seq_len);
-  cudaError_t e = kvp::tc_supported(dtype, s)
-                      ? kvp::launch_fam_tc(q, k, lse, dtype, s, sm_scale, window, heads, part,
-                                           workspace_bytes - target_heads_bytes(n_batch, h_q, seq_len), st,
-                                           (cudaStream_t)stream, 1)
-                      : kvp::launch_fam_simt(q, k, lse, dtype, s, sm_scale, window, heads,
-                                             (cudaStream_t)stream, 1);
+  cudaError_t e = tc ? kvp::launch_fam_tc(q, k, lse, dtype, s, sm_scale, window, heads, part,
+                                          workspace_bytes - target_heads_bytes(n_batch, h_q, seq_len), st,
+                                          (cudaStream_t)stream, 1)
+                     : kvp::launch_fam_simt(q, k, lse, dtype, s, sm_scale, window, heads,
+                                            (cudaStream_t)stream, 1);
   if (e != cudaSuccess) return cuda_fail(e, "kvp_future_attn_target launch");
   if (target || F) {
     e = kvp::launch_target_epilogue(heads, n_batch, h_q, h_kv, seq_len, window, eps, aggregate, target, F,
@@ -511,6 +586,17 @@ int kvp_decode_attn_noalloc(const void* q, const void* kc, const void* vc, int d
                 "this shape needs %zu bytes of scratch; the built-in scratch of "
                 "kvp_decode_attn_noalloc holds %zu (use kvp_decode_attn with a workspace)",
                 plan.total_bytes, (size_t)KVP_DECODE_NOALLOC_SCRATCH_BYTES);
+  if (!kvp::decode_noalloc_scratch_ready()) {
+    // The first call on a device (and context) looks up the scratch address, which a stream
+    // capture does not allow: ask for an uncaptured first call instead.
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t ce = cudaStreamIsCapturing((cudaStream_t)stream, &cs);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamIsCapturing");
+    if (cs != cudaStreamCaptureStatusNone)
+      return fail(KVP_ERR_INVALID_ARG,
+                  "kvp_decode_attn_noalloc: the first call on this device sets up its scratch address "
+                  "and cannot run under stream capture; make one call before capturing");
+  }
   void* scratch = nullptr;
   size_t scratch_bytes = 0;
   cudaError_t e = kvp::decode_noalloc_scratch(&scratch, &scratch_bytes);

@@ -11,9 +11,18 @@ namespace kvp {
 // Host-side count of kernel launches made by the library (diagnostics).
 void count_launches(int n);
 
+// Shape of a row-LSE / future-mass problem and the element strides of Q and K (batch, head,
+// token; the head_dim axis is contiguous).  Dense [n_batch, H, S, D] tensors have strides
+// (H*S*D, S*D, D).
 struct AttnShape {
   int n_batch, h_q, h_kv, seq_len, head_dim;
+  int64_t q_sb, q_sh, q_sr;
+  int64_t k_sb, k_sh, k_sr;
 };
+inline AttnShape dense_attn_shape(int n_batch, int h_q, int h_kv, int S, int D) {
+  const int64_t sd = (int64_t)S * D;
+  return AttnShape{n_batch, h_q, h_kv, S, D, sd * h_q, sd, D, sd * h_kv, sd, D};
+}
 
 // Running top-k mask of the sparse row LSE: static ranks and cutoffs [n_batch*h_kv, S].
 struct SparseMask {
@@ -29,8 +38,7 @@ struct SparseMask {
 // Workspace of the sparse row LSE on the tensor-core path (0 for the fp32 path).
 size_t sparse_lse_workspace_size(int dtype, AttnShape s);
 
-// fp32-FFMA tiled passes (any dtype; the only path for float32 inputs).  mask != null: the
-// sparse row LSE.
+// fp32-FFMA tiled passes: the path for float32 inputs.  mask != null: the sparse row LSE.
 cudaError_t launch_lse_simt(const void* q, const void* k, int dtype, AttnShape s, float scale,
                             float* lse, cudaStream_t st, const SparseMask* mask = nullptr);
 cudaError_t launch_fam_simt(const void* q, const void* k, const float* lse, int dtype, AttnShape s,
@@ -40,8 +48,9 @@ cudaError_t launch_target_epilogue(const float* F_heads, int n_batch, int h_q, i
                                    int window, float eps, int aggregate, float* target, float* F,
                                    cudaStream_t st);
 
-// tcgen05 / TMA passes (bf16 / f16, head_dim 128).
-bool tc_supported(int dtype, AttnShape s);
+// tcgen05 / TMA passes (bf16 / f16, head_dim 64 or 128).  tc_encoder_available() is false when
+// the driver's tensor-map encoder cannot be resolved (then these passes cannot run).
+bool tc_encoder_available();
 size_t fam_tc_workspace_size(AttnShape s, int window, int per_head = 0);
 cudaError_t launch_lse_tc(const void* q, const void* k, int dtype, AttnShape s, float scale,
                           float* lse, int* status, cudaStream_t st, const SparseMask* mask = nullptr);
@@ -116,8 +125,15 @@ cudaError_t launch_decode_mma(const void* q, const void* kc, const void* vc, int
                               int T_src, int accumulate, const DecodePlan& plan, void* ws,
                               int* status, cudaStream_t st);
 DecodePlan decode_plan(int n_layers, int h_q, int h_kv, int head_dim, int T_cap, int with_key_mass);
-// Static scratch of kvp_decode_attn_noalloc on the current device (set up on first use).
+// Static scratch of kvp_decode_attn_noalloc on the current device (set up on first use, and
+// again in a new context of the device).  _ready(): the address is already cached for the
+// current context.
+bool decode_noalloc_scratch_ready();
 cudaError_t decode_noalloc_scratch(void** ptr, size_t* bytes);
+// The calling thread's current CUDA context (a CUcontext; null when none is current or the
+// driver entry point cannot be resolved).  Keys the cached device addresses of the library's
+// static symbols.
+void* current_cu_context();
 cudaError_t launch_decode(const void* q, const void* kc, const void* vc, int dtype, int n_layers,
                           int h_q, int h_kv, int head_dim, int T_cap, const int32_t* len,
                           float scale, float* out, float* key_mass, const int32_t* key_pos,

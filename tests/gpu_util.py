@@ -42,3 +42,51 @@ def check_lse(lse_gpu, lse_ref, what=""):
     err = np.abs(np.asarray(lse_gpu, np.float64) - np.asarray(lse_ref, np.float64)).max()
     assert err <= LSE_ATOL, f"{what}: lse max abs err {err:.3e}"
     return float(err)
+
+
+def oracle_row_lse_threads(q, k, scale, rows_per_task=2048):
+    """oracle.row_lse over all rows, the rows split across host threads (numpy releases the
+    GIL in its matrix products and elementwise loops).  The oracle itself is unchanged: every
+    task is one call of it on a range of rows; q, k are converted to fp64 numpy once."""
+    import concurrent.futures as cf
+    import os
+
+    import oracle
+    q = np64(q) if isinstance(q, torch.Tensor) else np.asarray(q, np.float64)
+    k = np64(k) if isinstance(k, torch.Tensor) else np.asarray(k, np.float64)
+    Hq, S, _ = q.shape
+    G = Hq // k.shape[0]
+    out = np.empty((Hq, S))
+    tasks = [(h, r0) for h in range(Hq) for r0 in range(0, S, rows_per_task)]
+    tasks.sort(key=lambda t: -t[1])           # longest rows first
+
+    def run(t):
+        h, r0 = t
+        rows = np.arange(r0, min(S, r0 + rows_per_task))
+        out[h, rows] = oracle.row_lse(q[h:h + 1], k[h // G:h // G + 1], scale, rows=rows)[0]
+
+    with cf.ThreadPoolExecutor(max_workers=os.cpu_count() or 4) as ex:
+        list(ex.map(run, tasks))
+    return out
+
+
+def oracle_future_mass_threads(q, k, lse, scale, window, keys, keys_per_task=256):
+    """oracle.future_attn_mass on the listed keys, split across host threads (one oracle call
+    per key range)."""
+    import concurrent.futures as cf
+    import os
+
+    import oracle
+    q = np64(q) if isinstance(q, torch.Tensor) else np.asarray(q, np.float64)
+    k = np64(k) if isinstance(k, torch.Tensor) else np.asarray(k, np.float64)
+    keys = np.asarray(keys, np.int64)
+    F = np.empty((k.shape[0], keys.size))
+    spans = [(a, min(keys.size, a + keys_per_task)) for a in range(0, keys.size, keys_per_task)]
+
+    def run(sp):
+        a, b = sp
+        F[:, a:b] = oracle.future_attn_mass(q, k, lse, scale, window, keys=keys[a:b])
+
+    with cf.ThreadPoolExecutor(max_workers=os.cpu_count() or 4) as ex:
+        list(ex.map(run, spans))
+    return F

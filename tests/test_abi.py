@@ -62,18 +62,23 @@ def _bind(lib):
 def test_host_validation_codes(lib):
     L = _bind(lib)
     p = ctypes.c_void_p(4096)     # never dereferenced: validation fails first
-    assert L.kvp_abi_version() == 1
+    assert L.kvp_abi_version() == 2
     assert L.kvp_status_string(-6) == b"device-side range check failed"
     # null pointer
-    assert L.kvp_lse_pass(None, p, 1, 1, 4, 2, 16, 128, 0.1, p, None) == -1
+    assert L.kvp_lse_pass(None, p, 1, 1, 4, 2, 16, 128, None, None, 0.1, p, None) == -1
     # unsupported head_dim / dtype
-    assert L.kvp_lse_pass(p, p, 1, 1, 4, 2, 16, 96, 0.1, p, None) == -2
-    assert L.kvp_lse_pass(p, p, 7, 1, 4, 2, 16, 128, 0.1, p, None) == -2
+    assert L.kvp_lse_pass(p, p, 1, 1, 4, 2, 16, 96, None, None, 0.1, p, None) == -2
+    assert L.kvp_lse_pass(p, p, 7, 1, 4, 2, 16, 128, None, None, 0.1, p, None) == -2
     assert b"dtype" in L.kvp_last_error()
     # GQA mismatch, misalignment, negative window
-    assert L.kvp_lse_pass(p, p, 1, 1, 6, 4, 16, 128, 0.1, p, None) == -1
-    assert L.kvp_lse_pass(ctypes.c_void_p(4098), p, 1, 1, 4, 2, 16, 128, 0.1, p, None) == -1
-    assert L.kvp_future_attn_mass(p, p, p, 1, 1, 4, 2, 16, 128, 0.1, -1, p, None, 0, None) == -1
+    assert L.kvp_lse_pass(p, p, 1, 1, 6, 4, 16, 128, None, None, 0.1, p, None) == -1
+    assert L.kvp_lse_pass(ctypes.c_void_p(4098), p, 1, 1, 4, 2, 16, 128, None, None, 0.1, p, None) == -1
+    assert L.kvp_future_attn_mass(p, p, p, 1, 1, 4, 2, 16, 128, None, None, 0.1, -1, p, None, 0, None) == -1
+    # strides: not a multiple of 16 bytes, token stride below head_dim, non-positive
+    for bad in ((4096, 128, 12), (4096, 128, 64), (0, 0, 0)):
+        st = (ctypes.c_int64 * 3)(*bad)
+        assert L.kvp_lse_pass(p, p, 1, 2, 4, 2, 16, 128, st, None, 0.1, p, None) == -1
+        assert b"stride" in L.kvp_last_error()
     # select: stride < T, negative window sizes
     assert L.kvp_select_topk(p, 2, 100, 50, p, 4, 16, p, 64, p, None) == -1
     assert L.kvp_select_topk(p, 2, 100, 100, p, -1, 16, p, 64, p, None) == -1

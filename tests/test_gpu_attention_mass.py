@@ -180,3 +180,97 @@ def test_growing_logits_lse(kvp, step):
     if step < 10:
         F_r = oracle.future_attn_mass(q[0], k[0], lse_r, scale, 16)
         check_F(np64(F[0]), F_r, f"growing logits step {step}")
+
+
+def _fused_qkv(B, S, Hq, Hkv, D, dtype, seed):
+    """A fused QKV projection [B, S, (Hq + 2 Hkv) * D] and [B, H, S, D] views of its Q and K
+    slices (head_dim contiguous, token stride (Hq + 2 Hkv) * D)."""
+    gen = torch.Generator().manual_seed(seed)
+    Ht = Hq + 2 * Hkv
+    qkv = torch.randn(B, S, Ht, D, generator=gen).to(dtype)
+    q = qkv[:, :, :Hq].permute(0, 2, 1, 3)
+    k = qkv[:, :, Hq:Hq + Hkv].permute(0, 2, 1, 3)
+    return qkv, q, k
+
+
+@pytest.mark.parametrize("dtype,D,B", [(torch.bfloat16, 128, 1), (torch.float16, 64, 2),
+                                       (torch.bfloat16, 64, 1), (torch.float32, 128, 2)])
+def test_strided_fused_qkv_views(kvp, dtype, D, B):
+    """Q and K read in place from a fused QKV buffer (token-major, heads interleaved) through the
+    stride arguments: the same LSE and F as the oracle on dense copies, at a ragged S."""
+    S, Hq, Hkv, w = 700, 8, 2, 32
+    qkv, q, k = _fused_qkv(B, S, Hq, Hkv, D, dtype, seed=D + B)
+    qkv_d = qkv.cuda()
+    qv = qkv_d[:, :, :Hq].permute(0, 2, 1, 3)
+    kv = qkv_d[:, :, Hq:Hq + Hkv].permute(0, 2, 1, 3)
+    assert not qv.is_contiguous() and qv.stride(3) == 1 and qv.stride(2) == (Hq + 2 * Hkv) * D
+    scale = D ** -0.5
+    lse, F = _run(kvp, qv, kv, w)
+    for b in range(B):
+        lse_r, F_r = _oracle(q[b].contiguous(), k[b].contiguous(), w, scale)
+        check_lse(np64(lse[b]), lse_r, f"strided {dtype} D{D} b{b}")
+        check_F(np64(F[b]), F_r, f"strided {dtype} D{D} b{b}")
+    # the dense copies give the same result (the stride path changes only the addressing)
+    lse2, F2 = _run(kvp, qv.contiguous(), kv.contiguous(), w)
+    assert torch.equal(lse, lse2) and torch.equal(F, F2)
+
+
+def test_strided_sparse_lse_and_target(kvp):
+    """The sparse row LSE and the KVpop target take the same stride arguments."""
+    S, Hq, Hkv, D, w, n_sink, kk = 600, 4, 1, 128, 24, 4, 100
+    qkv, q, k = _fused_qkv(1, S, Hq, Hkv, D, torch.bfloat16, seed=11)
+    qkv_d = qkv.cuda()
+    qv = qkv_d[:, :, :Hq].permute(0, 2, 1, 3)
+    kv = qkv_d[:, :, Hq:Hq + Hkv].permute(0, 2, 1, 3)
+    ranks = kvp_inputs.make_static_ranks(1, S, seed=3).reshape(1, Hkv, S)
+    tau = kvp.kvp_topk_cutoffs(ranks.cuda(), n_sink, w, kk)
+    lse_s = kvp.kvp_sparse_lse_pass(qv, kv, ranks.cuda(), tau, n_sink, w)
+    lse_d = kvp.kvp_sparse_lse_pass(qv.contiguous(), kv.contiguous(), ranks.cuda(), tau, n_sink, w)
+    torch.cuda.synchronize()
+    kvp.kvp_check_device_status()
+    assert torch.equal(lse_s, lse_d)
+    tgt_s, Fh_s, _ = kvp.kvp_future_attn_target(qv, kv, lse_s, w, want=("target", "F_heads"))
+    tgt_d, Fh_d, _ = kvp.kvp_future_attn_target(qv.contiguous(), kv.contiguous(), lse_s, w,
+                                                want=("target", "F_heads"))
+    torch.cuda.synchronize()
+    assert torch.equal(Fh_s, Fh_d) and torch.equal(tgt_s, tgt_d)
+    scale = D ** -0.5
+    tau_r = oracle.fenwick_cutoffs(ranks.numpy().reshape(S), n_sink, w, kk)[None]
+    assert np.array_equal(tau.cpu().numpy().reshape(1, S), tau_r)
+    q0, k0 = q[0].contiguous(), k[0].contiguous()
+    lse_r = oracle.sparse_row_lse(q0, k0, ranks.numpy().reshape(Hkv, S), tau_r, scale, n_sink, w)
+    check_lse(np64(lse_s[0]), lse_r, "strided sparse LSE")
+    Fh_r = oracle.future_attn_mass_per_head(q0, k0, lse_r, scale, w)
+    check_F(np64(Fh_s[0]), Fh_r, "strided target F_heads")
+
+
+@pytest.mark.parametrize("dtype,D", [(torch.bfloat16, 128), (torch.float16, 64), (torch.bfloat16, 64)])
+def test_16bit_inputs_run_on_the_tensor_cores(kvp, dtype, D):
+    """bf16 / f16 inputs run on the tcgen05 passes at head_dim 64 and 128 (there is no fp32
+    fallback for them): on the Qwen3-4B-shaped layer the row-LSE pass runs faster than the
+    fp32 FFMA pipes could score its pairs even at a 2.2 GHz clock (SMs x 128 FMA lanes x 2
+    flops per clock), so the contraction ran on the tensor cores."""
+    w = kvp_inputs.QWEN3_4B_LAYER.scaled(head_dim=D, dtype={torch.bfloat16: "bf16", torch.float16: "f16"}[dtype])
+    x = kvp_inputs.make_prefill(w, device="cuda")
+    lse = torch.empty(1, w.h_q, w.seq_len, device="cuda")
+    for _ in range(3):
+        kvp.kvp_lse_pass(x["q"], x["k"], lse=lse)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    times = []
+    for _ in range(5):
+        ev[0].record()
+        kvp.kvp_lse_pass(x["q"], x["k"], lse=lse)
+        ev[1].record()
+        torch.cuda.synchronize()
+        times.append(ev[0].elapsed_time(ev[1]) * 1e-3)
+    kvp.kvp_check_device_status()
+    S = w.seq_len
+    flops = 2.0 * D * w.h_q * S * (S + 1) / 2
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ffma_peak = sms * 128 * 2 * 2.2e9
+    assert flops / min(times) > 2.0 * ffma_peak, (flops / min(times) / 1e12, ffma_peak / 1e12)
+    # and the result is the oracle's on a sampled head
+    scale = D ** -0.5
+    lse_r = oracle.row_lse(x["q"][0, :1].cpu(), x["k"][0, :1].cpu(), scale,
+                           rows=np.array([0, 1, 500, 4096, S - 1]))
+    check_lse(np64(lse[0, :1])[:, [0, 1, 500, 4096, S - 1]], lse_r, f"tc {dtype} D{D}")

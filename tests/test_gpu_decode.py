@@ -119,13 +119,19 @@ def test_decode_rejects_bad_length(kvp):
         kvp.kvp_check_device_status()
 
 
-@pytest.mark.parametrize("budget", [512, 4096])
-def test_qwen25_decode_eviction_full_size(kvp, budget):
-    """Qwen2.5-1.5B-shaped decode eviction at T = 120000 (28 layers, 12/2 heads, fp16):
-    control decode over the full cache with key mass, selection on that mass (4 sinks,
-    32 recent), compaction, pruned decode; checked per layer against the oracle."""
+@pytest.fixture(scope="module")
+def qwen25_cache():
+    return kvp_inputs.make_decode_cache(kvp_inputs.QWEN25_15B_DECODE, device="cuda")
+
+
+@pytest.mark.parametrize("budget", list(kvp_inputs.QWEN25_15B_DECODE.decode_budgets))
+def test_qwen25_decode_eviction_full_size(kvp, qwen25_cache, budget):
+    """Qwen2.5-1.5B-shaped decode eviction at T = 120000 (28 layers, 12/2 heads, fp16), at each
+    of the blog's budgets 512 / 1024 / 2048 / 4096: control decode over the full cache with key
+    mass, selection on that mass (4 sinks, 32 recent), compaction, pruned decode; selection of
+    all 56 rows bit-exact, the rest checked per layer against the oracle."""
     w = kvp_inputs.QWEN25_15B_DECODE
-    x = kvp_inputs.make_decode_cache(w, device="cuda")
+    x = qwen25_cache
     R, T, D = w.rows, w.seq_len, w.head_dim
     full_len = torch.full((R,), T, dtype=torch.int32, device="cuda")
     mass = torch.empty(R, T, device="cuda")
