@@ -9,7 +9,10 @@ HBM before the timed region; L2 is flushed (a 512 MiB write, then a 256 MiB read
 timed step.  `value` is the algorithmic TFLOP/s of the two QK^T passes over
 the whole step time.  A second measured object, `decode`, is the pruned-cache
 decode of the Qwen2.5-1.5B-shaped decode-eviction workload (28 layers,
-12/2 heads, fp16, T = 120000 cache pruned to 4096) in GB/s.
+12/2 heads, fp16, T = 120000 cache pruned to 4096) in GB/s, with every budget
+(512 / 1024 / 2048 / 4096) reported; `long_context` times the two passes at
+the Llama-3.1-8B-shaped 32 layers x S = 32768 and the Qwen3-8B-shaped
+S = 131072 workloads.
 
 --impl reference times the fp64 CPU oracle on a bounded sample of the same
 workload (the reference arm of this tier: there is no upstream code).
@@ -333,8 +336,11 @@ def run_kvp(args):
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"{peak_src} bf16_tflops (burst)"}
 
-    # pruned-cache decode on the decode-eviction workload (HBM bound)
+    # pruned-cache decode on the decode-eviction workload (HBM bound), every budget
     decode = decode_eviction_measure(kvp, dev, K, args.warmup, flush, peaks, ws)
+
+    # the two passes at the long-context workloads (32 layers x 32768; 131072)
+    long_context = long_context_measure(kvp, dev, args.warmup, peaks)
 
     # NEXT rows: KVpop target epilogue and the steady-state ring-cache decode step
     next_rows = {
@@ -352,7 +358,10 @@ def run_kvp(args):
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         f_c, t_c, cores, desc = oracle_sample_time(w)
         cpu = {"value": f_c / t_c / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-               "sample": desc, "seconds": t_c}
+               "sample": desc, "seconds": t_c, "nproc": os.cpu_count()}
+        t_1 = oracle_one_thread_time(w)
+        if t_1 is not None:
+            cpu["one_thread"] = {"value": f_c / t_1 / 1e12, "unit": "TFLOP/s", "seconds": t_1, "cores": 1}
     clk.__exit__(None, None, None)
     clocks = clk.summary()
     line = {
@@ -368,6 +377,7 @@ def run_kvp(args):
         "stages_ms": stage_mean,
         "roofline": roofline,
         "decode": decode,
+        "long_context": long_context,
         "next_rows": next_rows,
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -384,11 +394,22 @@ def run_kvp(args):
 
 
 def decode_eviction_measure(kvp, dev, K, W, flush, peaks, ws):
-    """Qwen2.5-1.5B decode eviction at T = 120000: control decode with key mass, select to 4096,
-    compact, pruned decode; the pruned decode's HBM GB/s is the reported figure."""
+    """Qwen2.5-1.5B decode eviction at T = 120000: control decode with key mass, select to the
+    budget, compact, pruned decode, at each of the blog's budgets (512 / 1024 / 2048 / 4096).
+    The pruned decode's HBM GB/s is the reported figure; the headline is the largest budget."""
     w = kvp_inputs.QWEN25_15B_DECODE
-    b = max(w.decode_budgets)
     x = kvp_inputs.make_decode_cache(w, device=dev)
+    per_budget = {}
+    for b in w.decode_budgets:
+        per_budget[str(b)] = _decode_eviction_budget(kvp, dev, K, W, flush, peaks, w, x, b)
+    head = dict(per_budget[str(max(w.decode_budgets))])
+    head["budgets"] = {b: {key: r[key] for key in ("value", "frac", "ms", "bytes")} | {
+        "select_topk_ms": r["other_stages"]["select_topk"]["ms"],
+        "compact_kv_ms": r["other_stages"]["compact_kv"]["ms"]} for b, r in per_budget.items()}
+    return head
+
+
+def _decode_eviction_budget(kvp, dev, K, W, flush, peaks, w, x, b):
     R, T, D = w.rows, w.seq_len, w.head_dim
     full_len = torch.full((R,), T, dtype=torch.int32, device=dev)
     mass = torch.empty(R, T, device=dev)
@@ -455,6 +476,79 @@ def decode_eviction_measure(kvp, dev, K, W, flush, peaks, ws):
             "compact_kv": {"ms": t_cmp, "GB/s": cmp_bytes / (t_cmp / 1e3) / 1e9},
         },
     }
+
+
+def long_context_measure(kvp, dev, W, peaks, K=3):
+    """The two passes at the long-context workloads, each pass timed with CUDA events:
+    Llama-3.1-8B-shaped 32 layers x S = 32768 (one launch per pass over all 32 layers,
+    2.81e14 flop) and the Qwen3-8B-shaped layer at S = 131072 (1.405e14 flop).  Their inputs
+    (8 GiB and 1 GiB of Q) are far larger than L2.  A pass runs for tens to hundreds of
+    milliseconds, so the fraction is also given against the sustained bf16 peak."""
+    res = {}
+    stream = torch.cuda.current_stream(dev)
+    for w in (kvp_inputs.LLAMA31_8B_32L, kvp_inputs.QWEN3_8B_131K):
+        x = kvp_inputs.make_prefill(w, device=dev)
+        q, k = x["q"], x["k"]
+        del x
+        B, S, D = w.n_layers, w.seq_len, w.head_dim
+        lse = torch.empty(B, w.h_q, S, device=dev)
+        F = torch.empty(B, w.h_kv, S, device=dev)
+        fws = torch.empty(kvp.kvp_future_attn_mass_workspace_size(q.dtype, B, w.h_q, w.h_kv, S, D, w.window),
+                          dtype=torch.uint8, device=dev)
+        for _ in range(W):
+            kvp.kvp_lse_pass(q, k, lse=lse)
+            kvp.kvp_future_attn_mass(q, k, lse, w.window, F=F, workspace=fws)
+        torch.cuda.synchronize(dev)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+        for e in evs:
+            e[0].record(stream)
+            kvp.kvp_lse_pass(q, k, lse=lse)
+            e[1].record(stream)
+            kvp.kvp_future_attn_mass(q, k, lse, w.window, F=F, workspace=fws)
+            e[2].record(stream)
+        torch.cuda.synchronize(dev)
+        kvp.kvp_check_device_status()
+        t_lse = sum(e[0].elapsed_time(e[1]) for e in evs) / K
+        t_fam = sum(e[1].elapsed_time(e[2]) for e in evs) / K
+        ww = S - w.window
+        f_lse = 2.0 * D * w.h_q * B * (S * (S + 1) // 2)
+        f_fam = 2.0 * D * w.h_q * B * (ww * (ww + 1) // 2)
+        tf = (f_lse + f_fam) / ((t_lse + t_fam) / 1e3) / 1e12
+        res[w.name] = {
+            "flops": f_lse + f_fam, "ms": t_lse + t_fam, "value": tf, "unit": "TFLOP/s",
+            "frac_burst": tf / float(peaks["bf16_tflops"]),
+            "frac_sustained": tf / float(peaks["bf16_tflops_sustained"]),
+            "lse_pass": {"ms": t_lse, "TFLOP/s": f_lse / (t_lse / 1e3) / 1e12},
+            "future_attn_mass": {"ms": t_fam, "TFLOP/s": f_fam / (t_fam / 1e3) / 1e12},
+            "steps": K, "l2": "inputs larger than L2"}
+        del q, k, lse, F, fws
+        torch.cuda.empty_cache()
+    return res
+
+
+def oracle_one_thread_time(w):
+    """The same oracle sample as oracle_sample_time, timed in a fresh process restricted to one
+    thread (one BLAS thread; numpy's elementwise loops are single-threaded anyway)."""
+    import numpy as np
+    x = kvp_inputs.make_prefill_layer(w, 0, device="cpu")
+    with tempfile.TemporaryDirectory(prefix="kvp_bench_") as d:
+        np.save(os.path.join(d, "q.npy"), x["q"][:1].to(torch.float64).numpy())
+        np.save(os.path.join(d, "k.npy"), x["k"][:1].to(torch.float64).numpy())
+        code = ("import sys, time, numpy as np\n"
+                f"sys.path.insert(0, {ROOT!r})\n"
+                "import oracle\n"
+                f"q = np.load({os.path.join(d, 'q.npy')!r}); k = np.load({os.path.join(d, 'k.npy')!r})\n"
+                f"s = {w.head_dim ** -0.5!r}\n"
+                "t = time.perf_counter()\n"
+                "l = oracle.row_lse(q, k, s)\n"
+                f"oracle.future_attn_mass(q, k, l, s, {w.window})\n"
+                "print(time.perf_counter() - t)\n")
+        env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+        res = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                             timeout=900)
+        if res.returncode != 0:
+            return None
+        return float(res.stdout.strip().splitlines()[-1])
 
 
 def target_measure(kvp, x, plan, w, K, W, flush, peak, stream, dev):

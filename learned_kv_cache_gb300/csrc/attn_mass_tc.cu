@@ -118,6 +118,7 @@ struct TcParams {
   const float* lse;      // mass pass: natural-log row LSE [B*Hq*S]
   float* out;            // LSE pass: lse [B*Hq*S]; mass pass: partial sums (workspace)
   int n_groups;          // LSE pass: B*Hq; mass pass: B*Hkv
+  int gblk;              // groups per block of the item order (decode_item)
   int NQT;               // LSE pass: query tiles per head
   int NT0, TPC, CMAX, NKT, Nf;   // mass pass schedule
   int per_head;          // mass pass: keep each query head's sum (partials [.., G, 2 halves, 128])
@@ -143,20 +144,31 @@ struct Item {
   int n_tiles;           // B tiles streamed by this CTA
 };
 
+// Work items are handed out in blocks of `gblk` groups: within a block the items of its groups
+// are interleaved, heaviest first; blocks follow each other.  So the CTAs resident at one time
+// work on a few groups whose streamed operand tiles (K for the LSE passes, Q for the mass
+// pass) overlap and stay in L2, however many layers one launch covers.
 template <int MODE>
 __device__ __forceinline__ Item decode_item(int I, const TcParams& p) {
   Item it;
   if (MODE != 1) {
-    it.group = I % p.n_groups;
-    it.tile = p.NQT - 1 - I / p.n_groups;
+    const int per_block = p.NQT * p.gblk;
+    const int blk = I / per_block, rem = I - blk * per_block;
+    const int gb = min(p.gblk, p.n_groups - blk * p.gblk);
+    it.group = blk * p.gblk + rem % gb;
+    it.tile = p.NQT - 1 - rem / gb;
     it.chunk = 0;
     it.per_head = 0;
     it.n_tiles = it.tile + 1;
   } else {
     const long long full_total = (long long)p.Nf * p.n_groups;
     if (I < full_total) {
-      int local = I / p.n_groups;
-      it.group = I % p.n_groups;
+      const long long per_block = (long long)p.Nf * p.gblk;
+      const int blk = (int)(I / per_block);
+      const int rem = (int)(I - blk * per_block);
+      const int gb = min(p.gblk, p.n_groups - blk * p.gblk);
+      int local = rem / gb;
+      it.group = blk * p.gblk + rem % gb;
       int c = 0;
       while (true) {
         const int n_c = p.NT0 - p.TPC * (c + 1) + 1;
@@ -916,6 +928,7 @@ cudaError_t launch_lse_tc(const void* q, const void* k, int dtype, AttnShape s, 
   p.c2 = scale * KVP_LOG2E;
   p.out = lse;
   p.n_groups = s.n_batch * s.h_q;
+  p.gblk = std::min(p.n_groups, 32);        // about one layer's query heads at a time
   p.NQT = (s.seq_len + BM - 1) / BM;
   p.status = status;
   const bool bf16 = dtype == KVP_BF16;
@@ -974,6 +987,7 @@ cudaError_t launch_fam_tc(const void* q, const void* k, const float* lse, int dt
   p.lse = lse;
   p.out = (float*)ws;
   p.n_groups = s.n_batch * s.h_kv;
+  p.gblk = std::min(p.n_groups, 8);         // about one layer's KV heads at a time
   p.NT0 = f.NT0;
   p.TPC = f.TPC;
   p.CMAX = f.CMAX;
