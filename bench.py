@@ -405,7 +405,10 @@ def decode_eviction_measure(kvp, dev, K, W, flush, peaks, ws):
     head = dict(per_budget[str(max(w.decode_budgets))])
     head["budgets"] = {b: {key: r[key] for key in ("value", "frac", "ms", "bytes")} | {
         "select_topk_ms": r["other_stages"]["select_topk"]["ms"],
-        "compact_kv_ms": r["other_stages"]["compact_kv"]["ms"]} for b, r in per_budget.items()}
+        "compact_kv_ms": r["other_stages"]["compact_kv"]["ms"],
+        "decode_in_chain_ms": r["eviction_step_chain"]["decode_in_chain_ms"],
+        "select_compact_decode_chain_ms": r["eviction_step_chain"]["select_compact_decode_ms"]}
+        for b, r in per_budget.items()}
     return head
 
 
@@ -466,8 +469,34 @@ def _decode_eviction_budget(kvp, dev, K, W, flush, peaks, w, x, b):
     sel_bytes = R * T * 4 + R * b * 4
     hbm = float(peaks["hbm_gbs"])
     gbs = dec_bytes / (t_dec / 1e3) / 1e9
+
+    # The eviction step as one stream: select -> compact -> pruned decode with nothing between the
+    # launches (each kernel starts while the one before finishes: programmatic dependent launch),
+    # L2 flushed before the selection; and the same chain without the decode.  Their difference is
+    # the decode's cost inside the step (it reads the cache compaction has just written).
+    def chain(with_decode):
+        ts = []
+        for _ in range(K):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            kvp.kvp_select_topk(mass, budgets, w.n_sink, w.n_recent, b, idx=idx, count=cnt)
+            kvp.kvp_compact_kv(x["k"], x["v"], idx, cnt, k_out=kc, v_out=vc)
+            if with_decode:
+                kvp.kvp_decode_attn(x["q"], kc, vc, cnt, out=out, workspace=ws_pr)
+            e1.record(stream)
+            ts.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        return sum(a.elapsed_time(z) for a, z in ts) / K
+
+    t_chain = chain(True)
+    t_chain0 = chain(False)
+    kvp.kvp_check_device_status()
     return {
         "workload": w.name, "budget": b, "metric": "pruned-cache decode HBM GB/s",
+        "eviction_step_chain": {"select_compact_decode_ms": t_chain, "select_compact_ms": t_chain0,
+                                "decode_in_chain_ms": t_chain - t_chain0,
+                                "l2": "flushed before the selection only"},
         "value": gbs, "unit": "GB/s", "frac": gbs / hbm, "peak": hbm,
         "ms": t_dec, "bytes": dec_bytes, "l2": "flushed before the pruned decode",
         "other_stages": {

@@ -24,6 +24,7 @@ __global__ void __launch_bounds__(256) compact_kernel(const uint4* __restrict__ 
                                                       const int32_t* __restrict__ count, int b_max,
                                                       uint4* __restrict__ ko, uint4* __restrict__ vo,
                                                       int* status) {
+  wait_prior_grid();                     // indices and counts may come from the kernel just before
   const long long total = (long long)R * b_max * VPR;
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += stride) {
@@ -57,8 +58,16 @@ cudaError_t compact(const void* k, const void* v, int R, int T, const int32_t* i
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   count_launches(1);
-  compact_kernel<VPR><<<(unsigned)blocks, 256, 0, st>>>((const uint4*)k, (const uint4*)v, R, T, idx,
-                                                        count, b_max, (uint4*)ko, (uint4*)vo, status);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, compact_kernel<VPR>, (const uint4*)k, (const uint4*)v, R, T, idx,
+                                     count, b_max, (uint4*)ko, (uint4*)vo, status);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -51,7 +51,8 @@ struct Dm {
   // range lies in one row (see decode_mma_plan), so the merge runs only after the last tile
   // has been consumed and no copy is in flight.
   static constexpr int OFF_SM = 0;
-  static constexpr int SCRATCH = (2 * DM_CWARPS * DM_QPAD + DM_CWARPS * DM_QPAD * D) * 4;
+  static constexpr int OSTR = D + 4;                        // padded row of the output scratch
+  static constexpr int SCRATCH = (3 * DM_CWARPS * DM_QPAD + DM_CWARPS * DM_QPAD * OSTR) * 4;
   static_assert(SCRATCH <= STAGES * STAGE_BYTES, "merge scratch must fit in the stage ring");
   static constexpr int OFF_CST = OFF_BAR + 128;             // merged state of this CTA
   static constexpr int OFF_FLAG = OFF_CST + PSTRIDE * 4;
@@ -172,7 +173,8 @@ __global__ void __launch_bounds__(DM_THREADS, 2)
   const uint32_t bar_empty = bar_full + 8 * C::STAGES;   // [STAGES]
   float* sm_m = reinterpret_cast<float*>(smem + C::OFF_SM);           // [4][8]
   float* sm_l = sm_m + DM_CWARPS * DM_QPAD;                           // [4][8]
-  float* sm_o = sm_l + DM_CWARPS * DM_QPAD;                           // [4][8][D]
+  float* sm_w = sm_l + DM_CWARPS * DM_QPAD;                           // [4][8] merge weights
+  float* sm_o = sm_w + DM_CWARPS * DM_QPAD;                           // [4][8][OSTR]
   volatile int* flags = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);  // [0] abort, [1] last
   float* cst = reinterpret_cast<float*>(smem + C::OFF_CST);          // m[8], l[8], o[8][D]
   float* sm_lg = reinterpret_cast<float*>(smem + C::OFF_LG);         // [keys of this CTA][8]
@@ -194,6 +196,8 @@ __global__ void __launch_bounds__(DM_THREADS, 2)
     cst[threadIdx.x] = -INFINITY;
     cst[DM_QPAD + threadIdx.x] = 0.f;
   }
+  // the cache, lengths and query may be written by the kernel just before this one
+  wait_prior_grid();
   __syncthreads();
 
   if (warp == DM_CWARPS) {
@@ -291,35 +295,40 @@ __global__ void __launch_bounds__(DM_THREADS, 2)
         sm_l[warp * DM_QPAD + 2 * t] = l0;
         sm_l[warp * DM_QPAD + 2 * t + 1] = l1;
       }
+      // query-head rows padded to OSTR floats: the four t-lanes of a g write distinct banks
 #pragma unroll
       for (int db = 0; db < C::KSTEPS; ++db) {
-        float* ow = sm_o + warp * DM_QPAD * D;
-        ow[(2 * t) * D + 16 * db + g] = o[db][0];
-        ow[(2 * t + 1) * D + 16 * db + g] = o[db][1];
-        ow[(2 * t) * D + 16 * db + g + 8] = o[db][2];
-        ow[(2 * t + 1) * D + 16 * db + g + 8] = o[db][3];
+        float* ow = sm_o + warp * DM_QPAD * C::OSTR;
+        ow[(2 * t) * C::OSTR + 16 * db + g] = o[db][0];
+        ow[(2 * t + 1) * C::OSTR + 16 * db + g] = o[db][1];
+        ow[(2 * t) * C::OSTR + 16 * db + g + 8] = o[db][2];
+        ow[(2 * t + 1) * C::OSTR + 16 * db + g + 8] = o[db][3];
       }
       asm volatile("bar.sync 1, %0;" ::"r"(DM_CWARPS * 32));
       float* part = p.cluster ? cst : p.partial + ((size_t)c * p.maxseg + seg) * C::PSTRIDE;
-      for (int e = ctid; e < DM_QPAD * D; e += DM_CWARPS * 32) {
-        const int qh = e / D, d = e % D;
+      if (ctid < DM_QPAD) {                  // per head: the merged max, the warps' weights, the sum
+        const int qh = ctid;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < DM_CWARPS; ++w) M = fmaxf(M, sm_m[w * DM_QPAD + qh]);
-        float L = 0.f, O = 0.f;
-        if (M != -INFINITY) {
+        float L = 0.f;
 #pragma unroll
-          for (int w = 0; w < DM_CWARPS; ++w) {
-            const float mw = sm_m[w * DM_QPAD + qh];
-            const float wgt = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
-            L = fmaf(sm_l[w * DM_QPAD + qh], wgt, L);
-            O = fmaf(sm_o[(w * DM_QPAD + qh) * D + d], wgt, O);
-          }
+        for (int w = 0; w < DM_CWARPS; ++w) {
+          const float mw = sm_m[w * DM_QPAD + qh];
+          const float wgt = (M == -INFINITY || mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
+          sm_w[w * DM_QPAD + qh] = wgt;
+          L = fmaf(sm_l[w * DM_QPAD + qh], wgt, L);
         }
-        if (d == 0) {
-          part[qh] = M;
-          part[DM_QPAD + qh] = L;
-        }
+        part[qh] = M;
+        part[DM_QPAD + qh] = L;
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(DM_CWARPS * 32));
+      for (int e = ctid; e < p.G * D; e += DM_CWARPS * 32) {    // padded heads carry no output
+        const int qh = e / D, d = e % D;
+        float O = 0.f;
+#pragma unroll
+        for (int w = 0; w < DM_CWARPS; ++w)
+          O = fmaf(sm_o[(w * DM_QPAD + qh) * C::OSTR + d], sm_w[w * DM_QPAD + qh], O);
         part[2 * DM_QPAD + qh * D + d] = O;
       }
       if (p.cluster) {                       // merged at the end through distributed shared memory
@@ -732,13 +741,14 @@ cudaError_t run(const void* q, const void* kc, const void* vc, int dtype, int n_
   cfg.blockDim = dim3(DM_THREADS);
   cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = p.cluster ? p.cluster : 1;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1] = pdl_attribute();
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   count_launches(1);
   e = cudaLaunchKernelEx(&cfg, kern, tk, tv, (const T*)q, p);
   if (e != cudaSuccess) return e;

@@ -13,6 +13,12 @@
 
 namespace kvp {
 
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization may
+// start while the previous kernel of the stream is finishing; it waits here, before its first
+// access to global memory, until that kernel has completed and its writes are visible (a no-op
+// when the launch was ordinary).
+__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Record the first device-side error in the per-device status word.
 __device__ __forceinline__ void raise_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);

@@ -11,6 +11,16 @@ namespace kvp {
 // Host-side count of kernel launches made by the library (diagnostics).
 void count_launches(int n);
 
+// Launch attribute that lets a kernel start while the previous kernel of its stream finishes
+// (programmatic dependent launch); the kernel must call wait_prior_grid() before it touches
+// global memory.
+inline cudaLaunchAttribute pdl_attribute() {
+  cudaLaunchAttribute a{};
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
 // Shape of a row-LSE / future-mass problem and the element strides of Q and K (batch, head,
 // token; the head_dim axis is contiguous).  Dense [n_batch, H, S, D] tensors have strides
 // (H*S*D, S*D, D).

@@ -125,6 +125,7 @@ __global__ void __launch_bounds__(SC_THREADS, 4) select_cluster_kernel(
   extern __shared__ __align__(16) uint8_t sc_raw[];
   SelShared& sh = *reinterpret_cast<SelShared*>(sc_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  wait_prior_grid();                     // the scores may come from the kernel just before
 
   const float* s = scores + (size_t)r * row_stride;
   const float* s_b = scores_b ? scores_b + (size_t)r * row_stride_b - n_a : nullptr;
@@ -571,6 +572,7 @@ __global__ void __launch_bounds__(SS_THREADS, 4) select_smem_kernel(
   extern __shared__ __align__(16) uint8_t ss_raw[];
   SmemSel& sh = *reinterpret_cast<SmemSel*>(ss_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  wait_prior_grid();                     // the scores may come from the kernel just before
 
   const float* s = scores + (size_t)r * row_stride;
   const float* s_b = scores_b ? scores_b + (size_t)r * row_stride_b - n_a : nullptr;
@@ -1021,13 +1023,14 @@ cudaError_t launch_select(const float* scores, int R, int T, int64_t row_stride,
   cfg.blockDim = dim3(in_smem ? SS_THREADS : SC_THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cl;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1] = pdl_attribute();
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   count_launches(1);
   const long long rs = (long long)row_stride, rsb = (long long)row_stride_b;
   const int na = scores_b ? n_a : T;
