@@ -125,7 +125,9 @@ int kvp_lse_pass(const void* q, const void* k, int dtype, int n_batch, int h_q, 
  * q, k (and their strides) as in kvp_lse_pass; lse is kvp_lse_pass's output.
  * F [n_batch, h_kv, seq_len] float32 (output).
  * workspace: device scratch of at least kvp_future_attn_mass_workspace_size()
- * bytes (partial sums of long key rows; may be NULL when that size is 0).
+ * bytes (partial sums, the query-side LSE operand, a work counter; may be NULL
+ * when that size is 0).  Calls that run at the same time need separate
+ * workspaces.
  * ------------------------------------------------------------------------- */
 size_t kvp_future_attn_mass_workspace_size(int dtype, int n_batch, int h_q, int h_kv,
                                            int seq_len, int head_dim, int window);

@@ -134,6 +134,9 @@ struct TcParams {
   const int32_t* inv;
   const int* perm_ok;
   int* status;
+  // persistent dense passes: the work-item counter (zero at launch) and the number of items
+  int* queue;
+  int total_items;
 };
 
 struct Item {
@@ -151,7 +154,15 @@ struct Item {
 template <int MODE>
 __device__ __forceinline__ Item decode_item(int I, const TcParams& p) {
   Item it;
-  if (MODE != 1) {
+  if (MODE == 2) {
+    // the sparse pass: plain heaviest-first order over every group (fewer live registers in a
+    // kernel that is short of them)
+    it.group = I % p.n_groups;
+    it.tile = p.NQT - 1 - I / p.n_groups;
+    it.chunk = 0;
+    it.per_head = 0;
+    it.n_tiles = it.tile + 1;
+  } else if (MODE == 0) {
     const int per_block = p.NQT * p.gblk;
     const int blk = I / per_block, rem = I - blk * per_block;
     const int gb = min(p.gblk, p.n_groups - blk * p.gblk);
@@ -292,22 +303,6 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
       tau_red[4 + warp] = vmin;
     }
   }
-  if (MODE == 1 && threadIdx.x < EPI_WARPS * 32) {
-    // The extra K-step adds -lse_i/scale (B side, three 16-bit parts) times 1 (A side) to every
-    // logit, so the accumulator already holds the LSE-offset logit.
-    const uint16_t one = bf16 ? 0x3F80u : 0x3C00u;
-    for (int e = threadIdx.x; e < 128 * EXT_K; e += EPI_WARPS * 32) {
-      const int r = e / EXT_K, k = e % EXT_K;
-      *reinterpret_cast<uint16_t*>(smem + L::OFF_AEXT + ext_off(r, k)) = k < 3 ? one : 0u;
-    }
-    // B side, per stage: rows 0..127 of k = 0..7 (written by TMA from the prepared array) at
-    // 16-byte row pitch, then the k = 8..15 half, which stays zero.
-    for (int e = threadIdx.x; e < NSTAGE * EXT_BYTES / 16; e += EPI_WARPS * 32) {
-      const int st = e / (EXT_BYTES / 16), off = (e % (EXT_BYTES / 16)) * 16;
-      if (off >= EXT_BYTES / 2) *reinterpret_cast<uint4*>(smem + L::OFF_BEXT + st * EXT_BYTES + off) = make_uint4(0u, 0u, 0u, 0u);
-    }
-    ptx::fence_proxy_async_smem();
-  }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -315,19 +310,11 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
 
   // Coordinates of the fixed A tile and of streamed tile t.  Q and K tensor maps are 4-D
   // (feature, token, head, batch); the A tile is (a_row, a_h, b_of_group).
-  int a_row, a_h, kv_z = 0, b_of_group = 0, hkv = 0;
-  if (MODE != 1) {
-    a_row = it.tile * BM;
-    b_of_group = it.group / p.Hq;
-    a_h = it.group % p.Hq;                    // query head
-    hkv = a_h / p.G;
-    kv_z = b_of_group * p.Hkv + hkv;
-  } else {
-    a_row = it.tile * BM;
-    b_of_group = it.group / p.Hkv;
-    hkv = it.group % p.Hkv;
-    a_h = hkv;                                // KV head
-  }
+  const int a_row = it.tile * BM;
+  const int b_of_group = it.group / p.Hq;
+  const int a_h = it.group % p.Hq;            // query head
+  const int hkv = a_h / p.G;
+  const int kv_z = b_of_group * p.Hkv + hkv;
   // Sparse pass, rank-ordered plan of a query tile whose rows all have a cutoff: the key tiles
   // holding the sinks and the protected windows in position order (eligible keys there are
   // dropped), then the keys in rank order up to the largest cutoff of the tile (eligible keys of
@@ -359,56 +346,35 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
     if (t < n_pos) return wt0 + (t - st_end);
     return -1;
   };
-  const int j0 = it.tile * BM;     // mass pass: first key of the tile
-  // mass pass: streamed tile t is query tile u of query head gh of the group (t = gh * per_head + u;
-  // both loops below keep (gh, u) as running counters instead of dividing)
-  // (row, head) of streamed tile t in its tensor map (the batch is b_of_group)
-  auto b_coords = [&](int t, int gh, int u, int& row, int& h) {
-    if (MODE != 1) {
-      const int kt = key_tile(t);
-      row = kt >= 0 ? kt * BN : (t - n_pos) * BN;
-      h = hkv;
-    } else {
-      row = j0 + p.window + BN * (it.chunk * p.TPC + u);
-      h = hkv * p.G + gh;
-    }
+  // token row of streamed key tile t in its tensor map (head hkv, batch b_of_group)
+  auto b_row = [&](int t) -> int {
+    const int kt = key_tile(t);
+    return kt >= 0 ? kt * BN : (t - n_pos) * BN;
   };
 
   if (warp == PRODUCER_WARP) {
-    const CUtensorMap* tmA = MODE != 1 ? &tmQ : &tmK;
-    const CUtensorMap* tmB = MODE != 1 ? &tmK : &tmQ;
     if (lane == 0) {
       ptx::mbar_arrive_expect_tx(bar_a, TILE_BYTES);
 #pragma unroll
       for (int hb = 0; hb < L::HALVES; ++hb)
-        ptx::tma_load_4d(sA + hb * HALF_BYTES, tmA, bar_a, 64 * hb, a_row, a_h, b_of_group);
+        ptx::tma_load_4d(sA + hb * HALF_BYTES, &tmQ, bar_a, 64 * hb, a_row, a_h, b_of_group);
     }
-    if (lane == 0) ptx::prefetch_tmap(&tmE);
-    int t = 0, pgh = 0, pu = 0;
+    if (MODE == 2 && lane == 0) ptx::prefetch_tmap(&tmE);
+    int t = 0;
     for (; t < it.n_tiles; ++t) {
       const int s = t % NSTAGE, use = t / NSTAGE;
-      const int gh = pgh, u = pu;
-      if (MODE == 1 && ++pu == it.per_head) {
-        pu = 0;
-        ++pgh;
-      }
       bool ok = true;
       if (use > 0) ok = ptx::mbar_wait(bar_empty + 8 * s, (use - 1) & 1, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, ok)) break;
       if (lane == 0) {
-        int row, h;
-        b_coords(t, gh, u, row, h);
+        const int row = b_row(t);
         const uint32_t dst = sB + s * TILE_BYTES;
-        // Mass pass: the stage also receives the 128 query rows' -lse/scale extension (three
-        // 16-bit parts per row, prepared in global memory) by its own TMA box.
-        ptx::mbar_arrive_expect_tx(bar_full + 8 * s, TILE_BYTES + (MODE == 1 ? EXT_BYTES / 2 : 0));
+        ptx::mbar_arrive_expect_tx(bar_full + 8 * s, TILE_BYTES);
         // sparse pass, rank-ordered tiles: the keys in rank order (third tensor map)
-        const CUtensorMap* src = (MODE == 2 && rank_mode && key_tile(t) < 0) ? &tmE : tmB;
+        const CUtensorMap* src = (MODE == 2 && rank_mode && key_tile(t) < 0) ? &tmE : &tmK;
 #pragma unroll
         for (int hb = 0; hb < L::HALVES; ++hb)
-          ptx::tma_load_4d(dst + hb * HALF_BYTES, src, bar_full + 8 * s, 64 * hb, row, h, b_of_group);
-        if (MODE == 1)
-          ptx::tma_load_3d(sBext + s * EXT_BYTES, &tmE, bar_full + 8 * s, 0, row, b_of_group * p.Hq + h);
+          ptx::tma_load_4d(dst + hb * HALF_BYTES, src, bar_full + 8 * s, 64 * hb, row, hkv, b_of_group);
       }
       if (MODE == 2) {
         // Per-column data of the tile for the epilogue's mask: the ranks of a position-ordered
@@ -459,9 +425,6 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
             const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
             ptx::mma_f16_ss(d, ptx::desc_sw128(sA + off), ptx::desc_sw128(bs + off), idesc, kk > 0);
           }
-          if (MODE == 1)
-            ptx::mma_f16_ss(d, ptx::desc_noswz(sAext, 128, 256), ptx::desc_noswz(sBext + s * EXT_BYTES, 2048, 128),
-                            idesc, 1);
           ptx::mma_commit(bar_empty + 8 * s);
           ptx::mma_commit(bar_accf + 8 * a);
         }
@@ -474,8 +437,7 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
     const int half = warp >> 2, quad = warp & 3;   // column group, TMEM lane quarter
     const int r = quad * 32 + lane;            // row of the A tile handled by this thread
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    uint64_t acc01 = 0, acc23 = 0;                           // mass pass: packed fp32 pairs
-    float m = -INFINITY, l = 0.f;                            // LSE pass running state
+    float m = -INFINITY, l = 0.f;                            // running state (base 2)
     const int row_i = it.tile * BM + r;                       // LSE passes: query of this row
     int tau_eff = INT_MAX;                                   // sparse LSE: cutoff (none: INT_MAX)
     if (MODE == 2) {
@@ -484,14 +446,8 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
     }
     bool ok = true;
     const uint64_t c2x2 = pack2(p.c2, p.c2);
-    int egh = 0, eu = 0;                                     // mass pass: (query head, tile) of t
     for (int t = 0; t < it.n_tiles; ++t) {
       const int a = t % NACC;
-      const int gh = egh, u = eu;
-      if (MODE == 1 && ++eu == it.per_head) {
-        eu = 0;
-        ++egh;
-      }
       if (!ptx::mbar_wait(bar_accf + 8 * a, (t / NACC) & 1, abort_flag, p.status)) { ok = false; break; }
       ptx::tc_fence_after();
       uint32_t v[CW];
@@ -506,7 +462,7 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar_acce + 8 * a);
 
-      if (MODE != 1) {
+      {
         const int kt = key_tile(t);
         const bool diag = (kt == it.tile);
         if (diag) {
@@ -630,38 +586,11 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
           }
           l += tile_sum(m);
         }
-      } else {
-        // the accumulator holds (q.k - lse_i/scale); past S it is -inf
-        const bool diag = (it.chunk == 0 && u == 0);
-        if (diag) {
-#pragma unroll
-          for (int c = 0; c < CW; ++c)
-            if (half * CW + c < r) v[c] = __float_as_uint(-INFINITY);
-        }
-        const uint64_t zero2 = 0;
-#pragma unroll
-        for (int c = 0; c < CW; c += 4) {
-          float x0, x1, x2, x3;
-          unpack2(ffma2(pack2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), c2x2, zero2), x0, x1);
-          unpack2(ffma2(pack2(__uint_as_float(v[c + 2]), __uint_as_float(v[c + 3])), c2x2, zero2), x2, x3);
-          acc01 = fadd2(acc01, pack2(fast_exp2(x0), fast_exp2(x1)));
-          acc23 = fadd2(acc23, pack2(fast_exp2(x2), fast_exp2(x3)));
-        }
-        if (p.per_head && u == it.per_head - 1) {   // last tile of this query head in the item
-          float f0, f1, f2, f3;
-          unpack2(acc01, f0, f1);
-          unpack2(acc23, f2, f3);
-          float* dst = p.out + ((((size_t)it.group * p.NKT + it.tile) * p.CMAX + it.chunk) * p.G + gh) * 2 * BM;
-          dst[half * BM + r] = (f0 + f1) + (f2 + f3);
-          acc01 = 0;
-          acc23 = 0;
-        }
-        __syncwarp();
       }
     }
     // Combine the two column halves of every row and write the result.
     asm volatile("bar.sync 1, %0;" ::"r"(EPI_WARPS * 32));
-    if (MODE != 1) {
+    {
       if (half > 0) {
         red[(half - 1) * 2 * BM + r] = m;
         red[(half - 1) * 2 * BM + BM + r] = l;
@@ -683,17 +612,6 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
         const int i = it.tile * BM + r;
         if (i < p.S) p.out[(size_t)it.group * p.S + i] = (M + __log2f(L)) * KVP_LN2;
       }
-    } else if (!p.per_head) {
-      float f0, f1, f2, f3;
-      unpack2(acc01, f0, f1);
-      unpack2(acc23, f2, f3);
-      const float f = (f0 + f1) + (f2 + f3);
-      if (half == 1) red[r] = f;
-      asm volatile("bar.sync 1, %0;" ::"r"(EPI_WARPS * 32));
-      if (half == 0 && ok && !*abort_flag && it.n_tiles > 0) {
-        float* dst = p.out + ((size_t)it.group * p.NKT + it.tile) * p.CMAX * BM + (size_t)it.chunk * BM;
-        dst[r] = f + red[r];
-      }
     }
   }
   ptx::tc_fence_before();
@@ -704,12 +622,315 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
   }
 }
 
-// F[group, j] = sum over the chunks of key tile j/128 of the partial sums, in chunk order.
+// ---------------------------------------------------------------- persistent mass pass
+// The future-mass pass as persistent CTAs (two per SM, every one resident) that take work items
+// from a global counter in the heaviest-first order of decode_item, so no CTA is set up per item:
+//  * warp 8 (producer): fetches items one ahead and publishes each through a 4-slot item ring,
+//    loads the item's key tile (A) once its buffer is free and streams its query tiles (B, with
+//    their -lse/scale extension box) through a 2-stage ring;
+//  * warp 9 (MMA, one thread): 128x128 tcgen05 products (+ the extension K-step) into two TMEM
+//    accumulators, tile T into accumulator T % 2;
+//  * warps 0-7 (epilogue): warp w reads TMEM lanes 32*(w%4).. and column half w/4 of every tile;
+//    each (row, half) keeps its own partial sum and writes it to the workspace, where the
+//    reduce kernel adds the halves and chunks in fixed order.
+// Measured against one CTA per work item: 2-3 % faster on the Qwen3-4B layer and at S = 131072
+// (the row-LSE pass measured slower in this form and keeps one CTA per item).  One CTA per SM
+// with two epilogue groups on alternate tiles and all four accumulators measured 30 % slower:
+// a single MMA stream per SM does not keep the tensor pipe busy.
+constexpr int P_EPI_WARPS = 8;
+constexpr int P_PRODUCER = P_EPI_WARPS;
+constexpr int P_MMA = P_EPI_WARPS + 1;
+constexpr int P_THREADS = 32 * (P_EPI_WARPS + 2);
+constexpr int P_CTAS_PER_SM = 2;
+constexpr int P_NACC = 2;                      // TMEM accumulators
+constexpr int P_NSTAGE = 2;                    // B tiles in flight
+constexpr int P_NITEM = 4;                     // published work items
+constexpr int P_TMEM_COLS = P_NACC * BN;       // 256
+constexpr int P_SLOTS = 2;                     // partial sums per row of an item: one per column half
+
+template <int HD>
+struct PSmem {
+  static constexpr int HALVES = HD / 64;
+  static constexpr int HALF_BYTES = 128 * 64 * 2;
+  static constexpr int TILE_BYTES = HALVES * HALF_BYTES;
+  static constexpr int OFF_A = 0;                                    // key tile
+  static constexpr int OFF_B = OFF_A + TILE_BYTES;                   // [P_NSTAGE] query tiles
+  static constexpr int OFF_BEXT = OFF_B + P_NSTAGE * TILE_BYTES;     // [P_NSTAGE] query-side extension
+  static constexpr int OFF_AEXT = OFF_BEXT + P_NSTAGE * EXT_BYTES;   // key-side extension
+  static constexpr int OFF_BAR = OFF_AEXT + EXT_BYTES;
+  static constexpr int OFF_MISC = OFF_BAR + 8 * (2 * P_NSTAGE + 2 * P_NACC + 2 + 2 * P_NITEM);
+  static constexpr int BYTES = OFF_MISC + 64 + 1024;                 // + alignment slack
+  static_assert(P_CTAS_PER_SM * (BYTES + 1024) <= 228 * 1024, "the CTAs of one SM must fit its shared memory");
+};
+
+template <int HD>
+__global__ void __launch_bounds__(P_THREADS, P_CTAS_PER_SM)
+    mass_tc_persistent_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                              const __grid_constant__ CUtensorMap tmE, const TcParams p, const bool bf16) {
+  using L = PSmem<HD>;
+  constexpr int TILE_BYTES = L::TILE_BYTES, HALF_BYTES = L::HALF_BYTES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s_base = ptx::smem_u32(smem);
+  const uint32_t sA = s_base + L::OFF_A, sB = s_base + L::OFF_B;
+  const uint32_t sAext = s_base + L::OFF_AEXT, sBext = s_base + L::OFF_BEXT;
+  const uint32_t bar_bfull = s_base + L::OFF_BAR;              // [P_NSTAGE]
+  const uint32_t bar_bempty = bar_bfull + 8 * P_NSTAGE;        // [P_NSTAGE]
+  const uint32_t bar_accf = bar_bempty + 8 * P_NSTAGE;         // [P_NACC]
+  const uint32_t bar_acce = bar_accf + 8 * P_NACC;             // [P_NACC]
+  const uint32_t bar_afull = bar_acce + 8 * P_NACC;
+  const uint32_t bar_aempty = bar_afull + 8;
+  const uint32_t bar_ifull = bar_aempty + 8;                   // [P_NITEM]
+  const uint32_t bar_iempty = bar_ifull + 8 * P_NITEM;         // [P_NITEM]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+  volatile int* ring = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 16);   // [P_NITEM]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P_NSTAGE; ++s) {
+      ptx::mbar_init(bar_bfull + 8 * s, 1);
+      ptx::mbar_init(bar_bempty + 8 * s, 1);
+    }
+    for (int a = 0; a < P_NACC; ++a) {
+      ptx::mbar_init(bar_accf + 8 * a, 1);
+      ptx::mbar_init(bar_acce + 8 * a, P_EPI_WARPS);
+    }
+    ptx::mbar_init(bar_afull, 1);
+    ptx::mbar_init(bar_aempty, 1);
+    for (int q = 0; q < P_NITEM; ++q) {
+      ptx::mbar_init(bar_ifull + 8 * q, 1);
+      ptx::mbar_init(bar_iempty + 8 * q, 2);                     // the MMA thread and the epilogue
+    }
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == P_MMA) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_holder), P_TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  if (threadIdx.x < P_EPI_WARPS * 32) {
+    // The extra K-step adds -lse_i/scale (B side, three 16-bit parts) times 1 (A side) to every
+    // logit, so the accumulator holds the LSE-offset logit: the key-side extension
+    // [1, 1, 1, 0, ...] is written once; of the query-side extension of every stage TMA writes
+    // the lower half (k = 0..7) and the upper half stays zero.
+    const uint16_t one = bf16 ? 0x3F80u : 0x3C00u;
+    for (int e = threadIdx.x; e < 128 * EXT_K; e += P_EPI_WARPS * 32) {
+      const int r = e / EXT_K, k = e % EXT_K;
+      *reinterpret_cast<uint16_t*>(smem + L::OFF_AEXT + ext_off(r, k)) = k < 3 ? one : 0u;
+    }
+    for (int e = threadIdx.x; e < P_NSTAGE * EXT_BYTES / 16; e += P_EPI_WARPS * 32) {
+      const int st = e / (EXT_BYTES / 16), off = (e % (EXT_BYTES / 16)) * 16;
+      if (off >= EXT_BYTES / 2) *reinterpret_cast<uint4*>(smem + L::OFF_BEXT + st * EXT_BYTES + off) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    ptx::fence_proxy_async_smem();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == P_PRODUCER) {
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmQ);
+      ptx::prefetch_tmap(&tmK);
+      ptx::prefetch_tmap(&tmE);
+      int next = atomicAdd(p.queue, 1);
+      long long T = 0;
+      int i = 0, last_a = -1;
+      for (;; ++i) {
+        const int slot = i % P_NITEM;
+        if (i >= P_NITEM && !ptx::mbar_wait(bar_iempty + 8 * slot, ((i / P_NITEM) - 1) & 1, abort_flag, p.status))
+          break;
+        const int I = next < p.total_items ? next : -1;
+        ring[slot] = I;
+        ptx::mbar_arrive(bar_ifull + 8 * slot);                 // release: the entry is visible
+        if (I < 0) break;
+        next = atomicAdd(p.queue, 1);                           // the following item, ahead of time
+        const Item it = decode_item<1>(I, p);
+        const int b_of_group = it.group / p.Hkv, hkv = it.group % p.Hkv;
+        if (i >= 1 && !ptx::mbar_wait(bar_aempty, (i - 1) & 1, abort_flag, p.status)) break;
+        ptx::mbar_arrive_expect_tx(bar_afull, TILE_BYTES);
+#pragma unroll
+        for (int hb = 0; hb < L::HALVES; ++hb)
+          ptx::tma_load_4d(sA + hb * HALF_BYTES, &tmK, bar_afull, 64 * hb, it.tile * BM, hkv, b_of_group);
+        last_a = i;
+        bool ok = true;
+        int gh = 0, u = 0;
+        for (int t = 0; t < it.n_tiles; ++t, ++T) {
+          const int s = (int)(T % P_NSTAGE);
+          if (T >= P_NSTAGE && !ptx::mbar_wait(bar_bempty + 8 * s, ((T / P_NSTAGE) - 1) & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          // streamed tile t is query tile u of query head gh of the group
+          const int row = it.tile * BM + p.window + BN * (it.chunk * p.TPC + u);
+          const int h = hkv * p.G + gh;
+          if (++u == it.per_head) {
+            u = 0;
+            ++gh;
+          }
+          const uint32_t dst = sB + s * TILE_BYTES;
+          ptx::mbar_arrive_expect_tx(bar_bfull + 8 * s, TILE_BYTES + EXT_BYTES / 2);
+#pragma unroll
+          for (int hb = 0; hb < L::HALVES; ++hb)
+            ptx::tma_load_4d(dst + hb * HALF_BYTES, &tmQ, bar_bfull + 8 * s, 64 * hb, row, h, b_of_group);
+          ptx::tma_load_3d(sBext + s * EXT_BYTES, &tmE, bar_bfull + 8 * s, 0, row, b_of_group * p.Hq + h);
+        }
+        if (!ok) break;
+      }
+      // copies still in flight land before the CTA can exit
+      if (last_a >= 0) ptx::mbar_wait_drain(bar_afull, last_a & 1, p.status);
+      for (long long q = T - P_NSTAGE < 0 ? 0 : T - P_NSTAGE; q < T; ++q)
+        ptx::mbar_wait_drain(bar_bfull + 8 * (int)(q % P_NSTAGE), (q / P_NSTAGE) & 1, p.status);
+    }
+  } else if (warp == P_MMA) {
+    if (lane == 0) {
+      const uint32_t idesc = ptx::idesc_f16(bf16, BM, BN);
+      long long T = 0;
+      for (int i = 0;; ++i) {
+        const int slot = i % P_NITEM;
+        if (!ptx::mbar_wait(bar_ifull + 8 * slot, (i / P_NITEM) & 1, abort_flag, p.status)) break;
+        const int I = ring[slot];
+        ptx::mbar_arrive(bar_iempty + 8 * slot);
+        if (I < 0) break;
+        const Item it = decode_item<1>(I, p);
+        if (!ptx::mbar_wait(bar_afull, i & 1, abort_flag, p.status)) break;
+        ptx::tc_fence_after();
+        bool ok = true;
+        for (int t = 0; t < it.n_tiles; ++t, ++T) {
+          const int s = (int)(T % P_NSTAGE), a = (int)(T % P_NACC);
+          if (!ptx::mbar_wait(bar_bfull + 8 * s, (T / P_NSTAGE) & 1, abort_flag, p.status) ||
+              (T >= P_NACC && !ptx::mbar_wait(bar_acce + 8 * a, ((T / P_NACC) - 1) & 1, abort_flag, p.status))) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t d = tmem + a * BN;
+          const uint32_t bs = sB + s * TILE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
+            ptx::mma_f16_ss(d, ptx::desc_sw128(sA + off), ptx::desc_sw128(bs + off), idesc, kk > 0);
+          }
+          ptx::mma_f16_ss(d, ptx::desc_noswz(sAext, 128, 256), ptx::desc_noswz(sBext + s * EXT_BYTES, 2048, 128),
+                          idesc, 1);
+          ptx::mma_commit(bar_bempty + 8 * s);
+          ptx::mma_commit(bar_accf + 8 * a);
+        }
+        if (!ok) break;
+        ptx::mma_commit(bar_aempty);                            // the key tile is free once these complete
+      }
+      // the last products must be complete before TMEM is released
+      if (T > 0) ptx::mbar_wait_drain(bar_accf + 8 * (int)((T - 1) % P_NACC), ((T - 1) / P_NACC) & 1, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int half = warp >> 2, quad = warp & 3;
+    constexpr int CW = BN / 2;
+    const int r = quad * 32 + lane;                             // key row of the A tile
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const uint64_t c2x2 = pack2(p.c2, p.c2);
+    long long T = 0;
+    for (int i = 0;; ++i) {
+      const int slot = i % P_NITEM;
+      const bool got = ptx::mbar_wait(bar_ifull + 8 * slot, (i / P_NITEM) & 1, abort_flag, p.status);
+      const int I = got ? ring[slot] : -1;
+      // every warp reads the entry before one thread releases it; a failed wait ends the loop
+      // of every epilogue warp together
+      if (ptx::bar_red_or(I < 0, 1, P_EPI_WARPS * 32)) break;
+      if (threadIdx.x == 0) ptx::mbar_arrive(bar_iempty + 8 * slot);
+      const Item it = decode_item<1>(I, p);
+      uint64_t acc01 = 0, acc23 = 0;                            // packed partial sums
+      // per query head: the head the accumulator holds (-1: none), the next unwritten head
+      int acc_head = -1, hd_next = 0;
+      float* part = p.out + ((((size_t)it.group * p.NKT + it.tile) * p.CMAX + it.chunk) *
+                             (p.per_head ? p.G : 1)) * P_SLOTS * BM;
+      auto write_head = [&](int h) {
+        float f0, f1, f2, f3;
+        unpack2(acc01, f0, f1);
+        unpack2(acc23, f2, f3);
+        for (; hd_next < h; ++hd_next) part[((size_t)hd_next * P_SLOTS + half) * BM + r] = 0.f;
+        part[((size_t)h * P_SLOTS + half) * BM + r] = (f0 + f1) + (f2 + f3);
+        hd_next = h + 1;
+        acc01 = 0;
+        acc23 = 0;
+      };
+      bool ok = true;
+      int gh = 0, u = 0;
+      for (int t = 0; t < it.n_tiles; ++t) {
+        const int tgh = gh, tu = u;
+        if (++u == it.per_head) {
+          u = 0;
+          ++gh;
+        }
+        const long long TT = T + t;
+        const int a = (int)(TT % P_NACC);
+        if (!ptx::mbar_wait(bar_accf + 8 * a, (TT / P_NACC) & 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        uint32_t v[CW];
+        {
+          const uint32_t taddr = tmem + lane_base + a * BN + half * CW;
+#pragma unroll
+          for (int h = 0; h < CW / 32; ++h)
+            ptx::tmem_ld32(taddr + 32 * h, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * h]));
+          ptx::tmem_ld_wait();
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar_acce + 8 * a);
+        if (p.per_head) {                                       // a new head: the previous one is complete
+          if (acc_head >= 0 && tgh != acc_head) write_head(acc_head);
+          acc_head = tgh;
+        }
+        // the accumulator holds (q.k - lse_i/scale); past S it is -inf
+        if (it.chunk == 0 && tu == 0) {                         // the window-diagonal tile: i >= j + w
+#pragma unroll
+          for (int c = 0; c < CW; ++c)
+            if (half * CW + c < r) v[c] = __float_as_uint(-INFINITY);
+        }
+        const uint64_t zero2 = 0;
+#pragma unroll
+        for (int c = 0; c < CW; c += 4) {
+          float x0, x1, x2, x3;
+          unpack2(ffma2(pack2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), c2x2, zero2), x0, x1);
+          unpack2(ffma2(pack2(__uint_as_float(v[c + 2]), __uint_as_float(v[c + 3])), c2x2, zero2), x2, x3);
+          acc01 = fadd2(acc01, pack2(fast_exp2(x0), fast_exp2(x1)));
+          acc23 = fadd2(acc23, pack2(fast_exp2(x2), fast_exp2(x3)));
+        }
+      }
+      if (ok) {
+        if (p.per_head) {
+          if (acc_head >= 0) write_head(acc_head);
+          for (; hd_next < p.G; ++hd_next) part[((size_t)hd_next * P_SLOTS + half) * BM + r] = 0.f;
+        } else {
+          float f0, f1, f2, f3;
+          unpack2(acc01, f0, f1);
+          unpack2(acc23, f2, f3);
+          part[(size_t)half * BM + r] = (f0 + f1) + (f2 + f3);
+        }
+      }
+      if (ptx::bar_red_or(!ok || *abort_flag != 0, 1, P_EPI_WARPS * 32)) break;
+      T += it.n_tiles;
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == P_MMA) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, P_TMEM_COLS);
+  }
+}
+
 // Query-side extension of the mass pass: row i of head z holds -lse[z, i]/scale split into three
 // 16-bit parts (exactly representable sum to ~2^-24 relative), then zeros; rows i >= S (the
 // padding the last query tiles read) hold -inf, so those queries get weight exactly 0.
 __global__ void ext_prep_kernel(const float* __restrict__ lse, int BHq, int S, int S_pad,
-                                float inv_scale, bool bf16, uint4* __restrict__ ext) {
+                                float inv_scale, bool bf16, uint4* __restrict__ ext, int* queue) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) *queue = 0;   // the mass pass's work counter
   const long long total = (long long)BHq * S_pad;
   for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
        e += (long long)gridDim.x * blockDim.x) {
@@ -754,6 +975,8 @@ __global__ void rank_scatter_keys_kernel(const uint16_t* __restrict__ k, long lo
   }
 }
 
+// F[group, j] = the partial sums of key tile j/128: its chunks in order, each chunk's two
+// column-half slots in order (deterministic).
 __global__ void __launch_bounds__(BM) fam_reduce_kernel(const float* __restrict__ part, int S, int NT0,
                                                         int TPC, int CMAX, int NKT,
                                                         float* __restrict__ F) {
@@ -762,14 +985,16 @@ __global__ void __launch_bounds__(BM) fam_reduce_kernel(const float* __restrict_
   if (j >= S) return;
   const int nt = max(0, NT0 - jt);
   const int nch = (nt + TPC - 1) / TPC;
-  const float* src = part + ((size_t)group * NKT + jt) * CMAX * BM + r;
+  const float* src = part + ((size_t)group * NKT + jt) * CMAX * P_SLOTS * BM + r;
   float f = 0.f;
-  for (int c = 0; c < nch; ++c) f += src[(size_t)c * BM];
+  for (int c = 0; c < nch; ++c)
+#pragma unroll
+    for (int q = 0; q < P_SLOTS; ++q) f += src[((size_t)c * P_SLOTS + q) * BM];
   F[(size_t)group * S + j] = f;
 }
 
-// F_heads[b, h*G + g, j] = sum over the chunks (and both column halves) of key tile j/128 of
-// query head g's partial sums, in chunk order.
+// F_heads[b, h*G + g, j] = query head g's partial sums of key tile j/128 (chunks in order, the
+// two slots of each in order).
 __global__ void __launch_bounds__(BM) fam_reduce_heads_kernel(const float* __restrict__ part, int S, int Hkv,
                                                               int G, int NT0, int TPC, int CMAX, int NKT,
                                                               float* __restrict__ F_heads) {
@@ -780,9 +1005,12 @@ __global__ void __launch_bounds__(BM) fam_reduce_heads_kernel(const float* __res
   const int nch = (nt + TPC - 1) / TPC;
   const int b = group / Hkv, h = group % Hkv;
   for (int g = 0; g < G; ++g) {
-    const float* src = part + (((size_t)group * NKT + jt) * CMAX * G + g) * 2 * BM + r;
     float f = 0.f;
-    for (int c = 0; c < nch; ++c) f += src[(size_t)c * G * 2 * BM] + src[(size_t)c * G * 2 * BM + BM];
+    for (int c = 0; c < nch; ++c) {
+      const float* src = part + ((((size_t)group * NKT + jt) * CMAX + c) * G + g) * P_SLOTS * BM + r;
+#pragma unroll
+      for (int q = 0; q < P_SLOTS; ++q) f += src[(size_t)q * BM];
+    }
     F_heads[((size_t)b * Hkv * G + h * G + g) * S + j] = f;
   }
 }
@@ -894,6 +1122,22 @@ cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
                         : launch_tc_hd<MODE, 128>(tq, tk, te, p, grid, bf16, st);
 }
 
+template <int HD>
+cudaError_t launch_mass_persistent_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& te,
+                                      const TcParams& p, bool bf16, cudaStream_t st) {
+  auto kern = mass_tc_persistent_kernel<HD>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PSmem<HD>::BYTES);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int slots = P_CTAS_PER_SM * sms;                        // every CTA resident at once
+  const int grid = p.total_items < slots ? p.total_items : slots;
+  count_launches(1);
+  kern<<<grid, P_THREADS, PSmem<HD>::BYTES, st>>>(tq, tk, te, p, bf16);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 bool tc_encoder_available() { return encode_fn() != nullptr; }
@@ -904,16 +1148,22 @@ size_t sparse_lse_workspace_size(int dtype, AttnShape s) {
   return ((n * 4 + 255) & ~(size_t)255) + ((n * s.head_dim * 2 + 255) & ~(size_t)255) + 256;
 }
 
-// Workspace of the mass pass: partial sums, then the query-side extension (16 bytes per query
-// row, S + 128 rows per query head).
+// Workspace of the mass pass: partial sums (P_SLOTS per row of every item chunk, per query head
+// in the per-head mode), the query-side extension (16 bytes per query row, S + 128 rows per
+// query head), then the work-item counter.
 size_t fam_partial_bytes(AttnShape s, const FamSched& f, int per_head) {
-  const size_t heads = per_head ? (size_t)2 * (s.h_q / s.h_kv) : 1;
-  return (((size_t)s.n_batch * s.h_kv * f.NKT * f.CMAX * heads * BM * sizeof(float)) + 255) & ~(size_t)255;
+  const size_t heads = per_head ? (size_t)(s.h_q / s.h_kv) : 1;
+  return (((size_t)s.n_batch * s.h_kv * f.NKT * f.CMAX * heads * P_SLOTS * BM * sizeof(float)) + 255) &
+         ~(size_t)255;
+}
+
+size_t fam_ext_bytes(AttnShape s) {
+  return (((size_t)s.n_batch * s.h_q * (s.seq_len + BN) * 16) + 255) & ~(size_t)255;
 }
 
 size_t fam_tc_workspace_size(AttnShape s, int window, int per_head) {
   const FamSched f = fam_schedule(s, window);
-  return fam_partial_bytes(s, f, per_head) + (size_t)s.n_batch * s.h_q * (s.seq_len + BN) * 16;
+  return fam_partial_bytes(s, f, per_head) + fam_ext_bytes(s) + 256;
 }
 
 cudaError_t launch_lse_tc(const void* q, const void* k, int dtype, AttnShape s, float scale,
@@ -999,6 +1249,7 @@ cudaError_t launch_fam_tc(const void* q, const void* k, const float* lse, int dt
   if (items > 0) {
     const int BHq = s.n_batch * s.h_q, S_pad = s.seq_len + BN;
     void* ext = (char*)ws + fam_partial_bytes(s, f, per_head);
+    int* queue = (int*)((char*)ext + fam_ext_bytes(s));
     CUtensorMap tq, tk, te;
     if (!make_q_tmap(&tq, q, dtype, s) || !make_k_tmap(&tk, k, dtype, s) ||
         !make_ext_tmap(&te, ext, dtype, BHq, S_pad))
@@ -1012,10 +1263,13 @@ cudaError_t launch_fam_tc(const void* q, const void* k, const float* lse, int dt
     if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
     count_launches(1);
     ext_prep_kernel<<<(unsigned)blocks, 256, 0, st>>>(lse, BHq, s.seq_len, S_pad, p.inv_scale,
-                                                     dtype == KVP_BF16, (uint4*)ext);
+                                                     dtype == KVP_BF16, (uint4*)ext, queue);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = launch_tc<1>(tq, tk, te, p, (int)items, dtype == KVP_BF16, s.head_dim, st);
+    p.queue = queue;
+    p.total_items = (int)items;
+    e = s.head_dim == 64 ? launch_mass_persistent_hd<64>(tq, tk, te, p, dtype == KVP_BF16, st)
+                         : launch_mass_persistent_hd<128>(tq, tk, te, p, dtype == KVP_BF16, st);
     if (e != cudaSuccess) return e;
   }
   count_launches(1);

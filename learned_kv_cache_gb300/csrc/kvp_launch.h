@@ -62,6 +62,7 @@ cudaError_t launch_target_epilogue(const float* F_heads, int n_batch, int h_q, i
 // the driver's tensor-map encoder cannot be resolved (then these passes cannot run).
 bool tc_encoder_available();
 size_t fam_tc_workspace_size(AttnShape s, int window, int per_head = 0);
+// mask == null: the dense row LSE; mask != null: the sparse row LSE.
 cudaError_t launch_lse_tc(const void* q, const void* k, int dtype, AttnShape s, float scale,
                           float* lse, int* status, cudaStream_t st, const SparseMask* mask = nullptr);
 // per_head = 1: F receives each query head's mass, [n_batch, h_q, seq_len].

@@ -71,6 +71,33 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Bounded wait that does not give up on the abort flag: used to let copies already in flight
+// land before a CTA exits (at most KVP_TC_TIMEOUT_NS, then it records a timeout and returns).
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer() - t0 > KVP_TC_TIMEOUT_NS) {
+      raise_status(status, KVP_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Named barrier `id` over `count` threads that also ORs a predicate across them (every thread
+// gets the same result): a decision all warps behind the barrier take together.
+__device__ __forceinline__ bool bar_red_or(bool pred, int id, int count) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred q, rp;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred rp, %2, %3, q;\n"
+      " selp.u32 %0, 1, 0, rp;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
