@@ -47,10 +47,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic of one launch of the dominant kernel from an ncu capture, valid only while the
 # kernel source is unchanged (sha256 of the .cu file at capture time).
 NCU_TRAFFIC = {
-    # ncu --set full of attn_tc_kernel<1> / <0> on the benchmark layer (S = 8192; the kernel source
-    # hashed below), DRAM bytes read + written per launch
-    "future_attn_mass": {"sha": "8928336e781a3540", "bytes": 130244608 + 3129600},
-    "lse_pass": {"sha": "8928336e781a3540", "bytes": 83914240 + 2356736},
+    # ncu --set full of the mass pass (mass_tc_persistent_kernel) and the row LSE pass
+    # (attn_tc_kernel<0>) on the benchmark layer (S = 8192; the kernel source hashed below),
+    # DRAM bytes read + written per launch
+    "future_attn_mass": {"sha": "9be214c52b59f476", "bytes": 116820224 + 3842816},
+    "lse_pass": {"sha": "9be214c52b59f476", "bytes": 83916288 + 2634240},
 }
 
 
