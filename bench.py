@@ -170,7 +170,12 @@ class ClockSampler:
 class L2Flush:
     """Evicts L2 between timed steps: writes 512 MiB (4x the 129 MB L2), then reads another
     256 MiB so the dirty lines of the write are written back during the flush and the next
-    timed kernel starts from a clean, cold L2."""
+    timed kernel starts from a clean, cold L2.  Then the GPU idles for ~100 us (a clock-count
+    delay kernel that touches no memory), so that the host has enqueued the timed launches
+    before the first of them can start: the events then bracket device work, not the Python
+    binding's and the launch path's host latency (the e2e leg keeps that latency in)."""
+
+    HEAD_START_CYCLES = 200_000
 
     def __init__(self, dev):
         self.w = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -179,6 +184,7 @@ class L2Flush:
     def __call__(self):
         self.w.zero_()
         self.r.sum()
+        torch.cuda._sleep(self.HEAD_START_CYCLES)
 
 
 def file_sha(path):
