@@ -38,6 +38,7 @@
 
 #include <algorithm>
 #include <climits>
+#include <cmath>
 #include <mutex>
 
 #include "kvp_common.cuh"
@@ -84,13 +85,22 @@ struct Smem {
   static constexpr int OFF_AEXT = OFF_MISC + 256;          // key-side extension: [1, 1, 1, 0, ...]
   static constexpr int OFF_BEXT = OFF_AEXT + EXT_BYTES;    // query-side extension per stage
   static constexpr int OFF_RED = OFF_BEXT + NSTAGE * EXT_BYTES;
-  static constexpr int OFF_RANK = OFF_AEXT;                // sparse LSE: rank ring (no extension)
+  // Sparse LSE (the mass pass's extension area is free there): the two operands of the masking
+  // K-step, [128 x 8] 16-bit rows of 16 bytes (A: one per query row; B: one per key of a stage),
+  // a zero block the descriptors read as k = 8..15, then the ring of per-tile column data.
+  static constexpr int SX_BYTES = 128 * 16;
+  static constexpr int OFF_SXA = OFF_AEXT;
+  static constexpr int OFF_SXB = OFF_SXA + SX_BYTES;                 // [NSTAGE]
+  static constexpr int OFF_SXZ = OFF_SXB + NSTAGE * SX_BYTES;
+  static constexpr int OFF_RANK = OFF_SXZ + SX_BYTES;
   // row-state exchange of the epilogue (NCG - 1 groups of [m | l] per row) + alignment slack
   static constexpr int BYTES = OFF_RED + (Epi<0>::NCG - 1) * 2 * BM * 4 + 1024;
 };
 // Sparse LSE pass: ranks of the last NRK key tiles (the extension operands are unused there).
 constexpr int NRK = 8;
-static_assert(NRK * BN * 4 <= Smem<128>::OFF_RED - Smem<128>::OFF_AEXT, "rank ring must fit in the extension area");
+static_assert(Smem<128>::OFF_RANK + NRK * BN * 4 <= Smem<128>::OFF_RED &&
+                  Smem<64>::OFF_RANK + NRK * BN * 4 <= Smem<64>::OFF_RED,
+              "masking operands and rank ring must fit in the extension area");
 
 // Byte offset of element (r, k) of a [128 x 16] K-major operand in 8 x 16-byte core matrices
 // (core (r/8, k/8) at (r/8)*256 + (k/8)*128): the layout desc_noswz(addr, 128, 256) reads.
@@ -133,6 +143,12 @@ struct TcParams {
   // order; *perm_ok is zero when the ranks were not a permutation (then every tile is dense).
   const int32_t* inv;
   const int* perm_ok;
+  // Rank-ordered tiles hold every key of rank <= the tile's largest cutoff, but only those at
+  // positions the position-ordered tiles do not cover count there.  The others are masked in the
+  // contraction: one more K = 16 step adds pen_a * pen_b (16-bit patterns of +2^a and -2^b,
+  // c2 * 2^(a+b) >= 2^20) to their logits, so exp2 of them is exactly 0 and the epilogue tests
+  // only the row's cutoff.  pen_a = 0: no masking step; the epilogue tests every key's position.
+  uint32_t pen_a, pen_b;
   int* status;
   // persistent dense passes: the work-item counter (zero at launch) and the number of items
   int* queue;
@@ -290,6 +306,14 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
     ptx::prefetch_tmap(&tmQ);
     ptx::prefetch_tmap(&tmK);
   }
+  if (MODE == 2 && p.pen_a != 0 && threadIdx.x < EPI_WARPS * 32) {
+    // masking operand, query side: every row [2^a, 0 x 7]; and the zero block (k = 8..15)
+    for (int e = threadIdx.x; e < 128; e += EPI_WARPS * 32) {
+      *reinterpret_cast<uint4*>(smem + L::OFF_SXA + 16 * e) = make_uint4(p.pen_a, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(smem + L::OFF_SXZ + 16 * e) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    ptx::fence_proxy_async_smem();
+  }
   int* tau_red = reinterpret_cast<int*>(smem + L::OFF_MISC + 16);      // sparse pass: [4] max, [4] min
   if (MODE == 2 && p.inv != nullptr && warp < 4) {
     // cutoff range over the query tile's rows (rows past S ignored)
@@ -322,6 +346,7 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
   // row.
   bool rank_mode = false;
   int st_end = 0, wt0 = 0, n_pos = 0;
+  const bool pen = MODE == 2 && p.pen_a != 0;
   if (MODE == 2 && p.inv != nullptr && *p.perm_ok) {
     const int i0 = it.tile * BM;
     const int tmax = max(max(tau_red[0], tau_red[1]), max(tau_red[2], tau_red[3]));
@@ -377,15 +402,42 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
           ptx::tma_load_4d(dst + hb * HALF_BYTES, src, bar_full + 8 * s, 64 * hb, row, hkv, b_of_group);
       }
       if (MODE == 2) {
-        // Per-column data of the tile for the epilogue's mask: the ranks of a position-ordered
-        // tile (dense plan), +inf ranks for the sink and window tiles of the rank-ordered plan,
-        // the positions of a rank-ordered tile.
+        // Per-column data of the tile: the ranks of a position-ordered tile for the epilogue's
+        // mask; of a rank-ordered tile, the masking step's B operand from the keys' positions.
+        // (Without the masking step: +inf ranks for the sink and window tiles of the rank-ordered
+        // plan and the positions of a rank-ordered tile, both for the epilogue.)
         const int kt = key_tile(t);
-        if (rank_mode && kt >= 0) {
+        if (rank_mode && kt < 0 && pen) {
+          // rank-ordered tile: a key outside [st_end, wt0) tiles is counted by a position-ordered
+          // tile (or lies past S): masked in the contraction through the B side of the masking
+          // step of this stage
+          const int kb = (t - n_pos) * BN + 4 * lane;
+          const int32_t* src = p.inv + (size_t)kv_z * p.S + kb;
+          int4 r4;
+          if (p.ranks_vec && kb + 3 < p.S) {
+            r4 = __ldg(reinterpret_cast<const int4*>(src));
+          } else {
+            r4.x = kb < p.S ? __ldg(src) : INT_MAX;
+            r4.y = kb + 1 < p.S ? __ldg(src + 1) : INT_MAX;
+            r4.z = kb + 2 < p.S ? __ldg(src + 2) : INT_MAX;
+            r4.w = kb + 3 < p.S ? __ldg(src + 3) : INT_MAX;
+          }
+          const int lo = st_end * BN, hi = wt0 * BN;
+          const uint32_t b0 = (r4.x < lo || r4.x >= hi) ? p.pen_b : 0u;
+          const uint32_t b1 = (r4.y < lo || r4.y >= hi) ? p.pen_b : 0u;
+          const uint32_t b2 = (r4.z < lo || r4.z >= hi) ? p.pen_b : 0u;
+          const uint32_t b3 = (r4.w < lo || r4.w >= hi) ? p.pen_b : 0u;
+          uint8_t* xb = smem + L::OFF_SXB + s * L::SX_BYTES + 16 * (4 * lane);
+          *reinterpret_cast<uint4*>(xb) = make_uint4(b0, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(xb + 16) = make_uint4(b1, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(xb + 32) = make_uint4(b2, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(xb + 48) = make_uint4(b3, 0u, 0u, 0u);
+          ptx::fence_proxy_async_smem();
+        } else if (rank_mode && kt >= 0 && !pen) {
           *reinterpret_cast<int4*>(rbuf + (t % NRK) * BN + 4 * lane) = make_int4(INT_MAX, INT_MAX, INT_MAX, INT_MAX);
         } else {
           const int kb = (kt >= 0 ? kt : t - n_pos) * BN + 4 * lane;
-          const int32_t* src = (rank_mode ? p.inv : p.ranks) + (size_t)kv_z * p.S + kb;
+          const int32_t* src = (rank_mode && kt < 0 ? p.inv : p.ranks) + (size_t)kv_z * p.S + kb;
           int4 r4;
           if (p.ranks_vec && kb + 3 < p.S) {
             r4 = __ldg(reinterpret_cast<const int4*>(src));
@@ -417,6 +469,9 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
           if (!ptx::mbar_wait(bar_full + 8 * s, (t / NSTAGE) & 1, abort_flag, p.status)) break;
           if (t >= NACC && !ptx::mbar_wait(bar_acce + 8 * a, ((t / NACC) - 1) & 1, abort_flag, p.status))
             break;
+          // rank-ordered tile with the masking step: its B operand is written by the producer
+          const bool xt = pen && rank_mode && key_tile(t) < 0;
+          if (xt && !ptx::mbar_wait(bar_rk + 8 * (t % NRK), (t / NRK) & 1, abort_flag, p.status)) break;
           ptx::tc_fence_after();
           const uint32_t d = tmem + a * BN;
           const uint32_t bs = sB + s * TILE_BYTES;
@@ -424,6 +479,12 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
           for (int kk = 0; kk < HD / 16; ++kk) {
             const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
             ptx::mma_f16_ss(d, ptx::desc_sw128(sA + off), ptx::desc_sw128(bs + off), idesc, kk > 0);
+          }
+          if (xt) {
+            // rows of 16 bytes (core matrices 128 bytes apart); k = 8..15 read from the zero block
+            const uint32_t xa = s_base + L::OFF_SXA, xb = s_base + L::OFF_SXB + s * L::SX_BYTES;
+            const uint32_t xz = s_base + L::OFF_SXZ;
+            ptx::mma_f16_ss(d, ptx::desc_noswz(xa, xz - xa, 128), ptx::desc_noswz(xb, xz - xb, 128), idesc, 1);
           }
           ptx::mma_commit(bar_empty + 8 * s);
           ptx::mma_commit(bar_accf + 8 * a);
@@ -470,7 +531,17 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
           for (int c = 0; c < CW; ++c)
             if (half * CW + c > r) v[c] = __float_as_uint(-INFINITY);
         }
-        if (MODE == 2 && rank_mode && kt < 0) {
+        if (MODE == 2 && rank_mode && kt < 0 && pen) {
+          // rank-ordered tile, keys outside the stream's position range already masked in the
+          // contraction: column c (rank rb + c) is kept when its rank is within the row's cutoff
+          const int cmax = tau_eff - ((t - n_pos) * BN + half * CW);
+          if (cmax < 0) continue;
+          if (cmax < CW - 1) {
+#pragma unroll
+            for (int c = 0; c < CW; ++c)
+              if (c > cmax) v[c] = 0xff800000u;
+          }
+        } else if (MODE == 2 && rank_mode && kt < 0) {
           // rank-ordered tile: column c holds the key of rank rb + c at position pos[c]; kept
           // when that key is eligible for the row and its rank is within the row's cutoff
           if (!ptx::mbar_wait(bar_rk + 8 * (t % NRK), (t / NRK) & 1, abort_flag, p.status)) {
@@ -492,9 +563,9 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
           }
         } else if (MODE == 2) {
           // Columns cs <= c <= cw are eligible (neither sink nor in the protected window) and
-          // are dropped when their rank is past the row's cutoff.  (The sink and window tiles of
-          // the rank-ordered plan carry rank +inf: their eligible keys are counted by the
-          // rank-ordered tiles.)
+          // are dropped when their rank is past the row's cutoff.  (Without the masking step the
+          // sink and window tiles of the rank-ordered plan carry rank +inf: their eligible keys
+          // are counted by the rank-ordered tiles.)
           const int jb = kt * BN + half * CW;
           const int cw = row_i - p.window - jb, cs = p.n_sink - jb;
           const int lo = cs > 0 ? cs : 0, hi = cw < CW - 1 ? cw : CW - 1;
@@ -579,7 +650,8 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
             t3 = max3(t3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
           }
           const float mn = fmaxf(m, fmaxf(fmaxf(t0, t1), fmaxf(t2, t3)) * p.c2);
-          if (mn == -INFINITY) continue;
+          // (a tile whose only finite scores carry the masking step's -2^20 counts as empty)
+          if (!(mn > (pen ? -0x1p19f : -INFINITY))) continue;
           if (mn > m) {
             l *= fast_exp2(m - mn);
             m = mn;
@@ -1166,6 +1238,21 @@ size_t fam_tc_workspace_size(AttnShape s, int window, int per_head) {
   return fam_partial_bytes(s, f, per_head) + fam_ext_bytes(s) + 256;
 }
 
+// Bit patterns of +2^a and -2^b for the sparse pass's masking step: a + b = e, the smallest e
+// with c2 * 2^e >= 2^20 (so a masked score's exp2 underflows to exactly 0 and the rounding of
+// c2 * 2^e stays far below one unit of the exponent).  Both 0 when 2^a or 2^b is not a normal
+// number of the operand type; the kernel then tests every key's position instead.
+void masking_step_bits(float c2, bool bf16, uint32_t* pa, uint32_t* pb) {
+  *pa = *pb = 0;
+  if (!(c2 > 0.f) || !std::isfinite(c2)) return;
+  const int e = (int)std::ceil(20.0 - std::log2((double)c2));
+  const int a = (int)std::floor(e / 2.0), b = e - a;
+  const int lo = bf16 ? -126 : -14, hi = bf16 ? 127 : 15;
+  if (a < lo || a > hi || b < lo || b > hi) return;
+  *pa = bf16 ? (uint32_t)(a + 127) << 7 : (uint32_t)(a + 15) << 10;
+  *pb = (bf16 ? (uint32_t)(b + 127) << 7 : (uint32_t)(b + 15) << 10) | 0x8000u;
+}
+
 cudaError_t launch_lse_tc(const void* q, const void* k, int dtype, AttnShape s, float scale,
                           float* lse, int* status, cudaStream_t st, const SparseMask* mask) {
   CUtensorMap tq, tk;
@@ -1216,6 +1303,7 @@ cudaError_t launch_lse_tc(const void* q, const void* k, int dtype, AttnShape s, 
       return cudaErrorInvalidValue;
     p.inv = mask->inv;
     p.perm_ok = mask->perm_ok;
+    masking_step_bits(p.c2, bf16, &p.pen_a, &p.pen_b);
     return launch_tc<2>(tq, tk, tks, p, p.n_groups * p.NQT, bf16, s.head_dim, st);
   }
   return launch_tc<0>(tq, tk, tk, p, p.n_groups * p.NQT, bf16, s.head_dim, st);

@@ -74,6 +74,47 @@ def test_sparse_lse_matches_oracle(kvp, dtype, D, S, Hq, Hkv, s, w, k):
         assert np.abs(np64(lse[0]) - dense).max() < 1e-3
 
 
+@pytest.mark.parametrize("dtype,D,scale", [
+    ("bf16", 128, None),     # rank-ordered tiles mask out-of-range keys in the contraction
+    ("f16", 128, None),
+    ("f16", 64, None),
+    ("bf16", 128, 1e-4),     # a small scale: the masking step's factors are still bf16 normals
+    ("f16", 128, 1e-4),      # 2^a * 2^b out of f16's range: every key's position tested instead
+])
+def test_sparse_lse_rank_ordered_stream(kvp, dtype, D, scale):
+    """A small long-range budget (k = 80 of 3000) so most query tiles take the rank-ordered
+    stream.  Keys planted after a query with a large logit for it (a multiple of that query)
+    are ranked first, so they sit in the first rank-ordered tiles of every earlier query tile,
+    where only the mask removes them: a missed key adds e^(~100) to its row."""
+    S, Hq, Hkv, s, w, k = 3000, 4, 2, 4, 64, 80
+    gen = torch.Generator().manual_seed(D + (0 if scale is None else 1))
+    dt = kvp_inputs.torch_dtype(dtype)
+    q = torch.randn(1, Hq, S, D, generator=gen)
+    kk = torch.randn(1, Hkv, S, D, generator=gen)
+    G = Hq // Hkv
+    planted = torch.randint(1500, S, (Hkv, 6), generator=gen)
+    for h in range(Hkv):
+        for j in planted[h].tolist():
+            kk[0, h, j] = q[0, h * G, j - 600] * 2.0
+    q, kk = q.to(dt), kk.to(dt)
+    ranks = kvp_inputs.make_static_ranks(Hkv, S, seed=D)
+    for h in range(Hkv):                        # planted keys take the smallest ranks
+        pl = planted[h].unique()
+        rest = torch.ones(S, dtype=torch.bool)
+        rest[pl] = False
+        order = ranks[h].argsort()
+        order = order[rest[order]]              # the other keys keep their relative order
+        ranks[h, pl] = torch.arange(len(pl), dtype=ranks.dtype)
+        ranks[h, order] = torch.arange(len(pl), S, dtype=ranks.dtype)
+    sc = D ** -0.5 if scale is None else scale
+    tau = kvp.kvp_topk_cutoffs(ranks.cuda(), s, w, k)
+    lse = kvp.kvp_sparse_lse_pass(q.cuda(), kk.cuda(), ranks.cuda(), tau, s, w, sm_scale=sc)
+    torch.cuda.synchronize()
+    kvp.kvp_check_device_status()
+    want = oracle.sparse_row_lse(q[0], kk[0], ranks.numpy(), tau.cpu().numpy(), sc, s, w)
+    check_lse(np64(lse[0]), want, f"{dtype} D{D} scale {scale}")
+
+
 def test_future_mass_from_sparse_lse(kvp):
     dtype, D, S, Hq, Hkv, s, w, k = "bf16", 128, 900, 4, 2, 4, 32, 200
     q, kk, ranks, tau, lse = _sparse_case(kvp, dtype, D, S, Hq, Hkv, s, w, k, seed=11)
