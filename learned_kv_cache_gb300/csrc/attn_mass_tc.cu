@@ -149,6 +149,9 @@ struct TcParams {
   // c2 * 2^(a+b) >= 2^20) to their logits, so exp2 of them is exactly 0 and the epilogue tests
   // only the row's cutoff.  pen_a = 0: no masking step; the epilogue tests every key's position.
   uint32_t pen_a, pen_b;
+  // a query tile takes the rank-ordered stream when it streams fewer than rank_bias_pct percent
+  // of the dense causal row's tiles
+  int rank_bias_pct;
   int* status;
   // persistent dense passes: the work-item counter (zero at launch) and the number of items
   int* queue;
@@ -358,7 +361,7 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
       st_end = sink_tiles < wt0 ? sink_tiles : wt0;
       n_pos = st_end + (it.tile - wt0 + 1);
       const int n_rank = tmax / BN + 1;
-      if (n_pos + n_rank < it.tile + 1) {
+      if ((n_pos + n_rank) * 100 < (it.tile + 1) * p.rank_bias_pct) {
         rank_mode = true;
         it.n_tiles = n_pos + n_rank;
       }
@@ -1304,6 +1307,11 @@ cudaError_t launch_lse_tc(const void* q, const void* k, int dtype, AttnShape s, 
     p.inv = mask->inv;
     p.perm_ok = mask->perm_ok;
     masking_step_bits(p.c2, bf16, &p.pen_a, &p.pen_b);
+    // With the masking step a rank-ordered tile costs less than a dense one with its per-score
+    // rank test, so the rank-ordered stream pays even when it is somewhat longer (Qwen3-4B layer,
+    // k = 1916 of 8192: 0.220 / 0.214 / 0.214 / 0.216 / 0.222 ms at 100 / 130 / 160 / 200 / 260 %).
+    // Without it (pen_a = 0) a rank-ordered tile tests every key's position: shorter streams only.
+    p.rank_bias_pct = p.pen_a != 0 ? 130 : 100;
     return launch_tc<2>(tq, tk, tks, p, p.n_groups * p.NQT, bf16, s.head_dim, st);
   }
   return launch_tc<0>(tq, tk, tk, p, p.n_groups * p.NQT, bf16, s.head_dim, st);
