@@ -848,10 +848,46 @@ def ring_step_measure(kvp, dev, K, W, flush, peaks, cap=4096):
     dec_bytes = 2 * R * cap * D * elt + x["q"].numel() * elt + out.numel() * 4 + R * cap * 8
     hbm = float(peaks["hbm_gbs"])
     gbs = (ins_bytes + dec_bytes) / ((t_ins + t_dec) / 1e3) / 1e9
-    return {"metric": "ring-cache decode step HBM GB/s", "value": gbs, "unit": "GB/s",
-            "frac": gbs / hbm, "peak": hbm, "cap": cap, "us_per_token": (t_ins + t_dec) * 1e3,
-            "ring_insert_us": t_ins * 1e3, "decode_with_key_mass_us": t_dec * 1e3,
-            "bytes": ins_bytes + dec_bytes, "l2": "flushed before every token step"}
+
+    # The token loop as it runs in serving: token steps back to back, round-robin over n_c
+    # independent ring caches (sequences) whose total is more than 2.5x L2, so every step reads
+    # its cache from HBM; the average per token leaves out the per-measurement event overhead.
+    state_bytes = 2 * R * cap * D * elt + R * cap * 8
+    n_c = max(3, -(-int(2.5 * L2_BYTES) // state_bytes) + 1)
+    seqs = [(kc.clone(), vc.clone(), pos.clone(), score.clone(), fill.clone()) for _ in range(n_c)]
+    n_tok = max(30, 3 * n_c)
+    nk = torch.randn(n_tok, R, D, generator=g, device=dev).to(kc.dtype)
+    nv = torch.randn(n_tok, R, D, generator=g, device=dev).to(kc.dtype)
+
+    def tokens(t0):
+        for i in range(n_tok):
+            ck, cv, cp, cs, cf = seqs[i % n_c]
+            kvp.kvp_ring_insert(ck, cv, cp, cs, cf, nk[i], nv[i], t0 + i // n_c, w.n_sink,
+                                w.n_recent, out_slot=slot)
+            kvp.kvp_decode_attn(x["q"], ck, cv, cf, out=out, key_mass=cs, accumulate=True,
+                                workspace=ws)
+
+    tokens(cap + steps)
+    t_loop = 0.0
+    for rep in range(3):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        tokens(cap + steps + (rep + 1) * n_tok)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        t_loop += e0.elapsed_time(e1) / n_tok / 3
+    del seqs
+    kvp.kvp_check_device_status()
+    gbs_loop = (ins_bytes + dec_bytes) / (t_loop / 1e3) / 1e9
+    return {"metric": "ring-cache decode step HBM GB/s", "value": gbs_loop, "unit": "GB/s",
+            "frac": gbs_loop / hbm, "peak": hbm, "cap": cap, "us_per_token": t_loop * 1e3,
+            "bytes": ins_bytes + dec_bytes,
+            "timing": f"token loop: {n_tok} token steps back to back, round-robin over {n_c} ring "
+                      f"caches ({n_c * state_bytes / 1e6:.0f} MB > L2), average per token",
+            "isolated": {"value": gbs, "frac": gbs / hbm, "us_per_token": (t_ins + t_dec) * 1e3,
+                         "ring_insert_us": t_ins * 1e3, "decode_with_key_mass_us": t_dec * 1e3,
+                         "l2": "flushed before every token step, each launch timed"}}
 
 
 def e2e_measure(kvp, x, plan, budgets, w, K, W, stream, flops, ws, dev):

@@ -71,10 +71,12 @@ def test_eviction_auc_from_future_mass(kvp):
             assert auc[r, m].item() >= auc_opt[r, 0].item()
 
 
-@pytest.mark.parametrize("R,M,T", [(2, 3, 1), (1, 2, 8191), (3, 5, 20003), (2, 4, 16388)])
+@pytest.mark.parametrize("R,M,T", [(2, 3, 1), (1, 2, 8191), (3, 5, 20003), (2, 4, 16388),
+                                   (8, 8, 20003), (4, 16, 16388), (16, 4, 5), (8, 16, 131072)])
 def test_eviction_auc_shapes(kvp, R, M, T):
     """Scalar path (T not a multiple of 4), several 8192-entry chunks with a ragged tail, the
-    vector path with a 4-entry tail chunk, a single entry; F spans many binades."""
+    vector path with a 4-entry tail chunk, a single entry, many rankings of short rows, and the
+    16-ranking benchmark shape; F spans many binades."""
     gen = torch.Generator(device="cuda").manual_seed(R * 1000 + T)
     F = torch.exp(4.0 * torch.randn(R, T, generator=gen, device="cuda")) * 1e-3
     rk = torch.stack([torch.stack([torch.randperm(T, generator=gen, device="cuda") for _ in range(M)])
