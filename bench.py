@@ -51,8 +51,8 @@ NCU_TRAFFIC = {
     # ncu --set full of the mass pass (mass_tc_persistent_kernel) and the row LSE pass
     # (attn_tc_kernel<0>) on the benchmark layer (S = 8192; the kernel source hashed below),
     # DRAM bytes read + written per launch
-    "future_attn_mass": {"sha": "9be214c52b59f476", "bytes": 116820224 + 3842816},
-    "lse_pass": {"sha": "9be214c52b59f476", "bytes": 83916288 + 2634240},
+    "future_attn_mass": {"sha": "00ee4da619f9519e", "bytes": 115552256 + 3821568},
+    "lse_pass": {"sha": "00ee4da619f9519e", "bytes": 83914496 + 2335232},
 }
 
 
