@@ -627,9 +627,10 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
         // key the tile is summed against the current m without taking its max; only a sum that
         // reaches 2^64 (a term near overflow) sends the tile through the exact path (tile max,
         // rescale of l, sum), and l is brought back below 2^32 by exact power-of-two steps of m.
-        // Terms that underflow against m are below 2^-126 of l >= 1.  (The sparse pass, short of
-        // registers, always takes the exact path.)
-        bool exact = MODE == 2 || m == -INFINITY;
+        // Terms that underflow against m are below 2^-126 of l >= 1.  In the sparse pass a score
+        // masked by the masking step (about -2^20 after scaling) adds exactly 0 against any m a
+        // kept key has set.
+        bool exact = m == -INFINITY;
         if (!exact) {
           const float ts = tile_sum(m);
           if (ts < 0x1p64f) {
