@@ -805,6 +805,7 @@ __global__ void __launch_bounds__(P_THREADS, P_CTAS_PER_SM)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  wait_prior_grid();                     // the extension rows and the queue come from ext_prep
 
   if (warp == P_PRODUCER) {
     if (lane == 0) {
@@ -1006,6 +1007,7 @@ __global__ void __launch_bounds__(P_THREADS, P_CTAS_PER_SM)
 // padding the last query tiles read) hold -inf, so those queries get weight exactly 0.
 __global__ void ext_prep_kernel(const float* __restrict__ lse, int BHq, int S, int S_pad,
                                 float inv_scale, bool bf16, uint4* __restrict__ ext, int* queue) {
+  wait_prior_grid();                     // lse may come from the kernel just before
   if (blockIdx.x == 0 && threadIdx.x == 0) *queue = 0;   // the mass pass's work counter
   const long long total = (long long)BHq * S_pad;
   for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
@@ -1056,6 +1058,7 @@ __global__ void rank_scatter_keys_kernel(const uint16_t* __restrict__ k, long lo
 __global__ void __launch_bounds__(BM) fam_reduce_kernel(const float* __restrict__ part, int S, int NT0,
                                                         int TPC, int CMAX, int NKT,
                                                         float* __restrict__ F) {
+  wait_prior_grid();
   const int jt = blockIdx.x, group = blockIdx.y, r = threadIdx.x;
   const int j = jt * BM + r;
   if (j >= S) return;
@@ -1074,6 +1077,7 @@ __global__ void __launch_bounds__(BM) fam_reduce_kernel(const float* __restrict_
 __global__ void __launch_bounds__(BM) fam_reduce_heads_kernel(const float* __restrict__ part, int S, int Hkv,
                                                               int G, int NT0, int TPC, int CMAX, int NKT,
                                                               float* __restrict__ F_heads) {
+  wait_prior_grid();
   const int jt = blockIdx.x, group = blockIdx.y, r = threadIdx.x;
   const int j = jt * BM + r;
   if (j >= S) return;
@@ -1210,8 +1214,7 @@ cudaError_t launch_mass_persistent_hd(const CUtensorMap& tq, const CUtensorMap& 
   const int slots = P_CTAS_PER_SM * sms;                        // every CTA resident at once
   const int grid = p.total_items < slots ? p.total_items : slots;
   count_launches(1);
-  kern<<<grid, P_THREADS, PSmem<HD>::BYTES, st>>>(tq, tk, te, p, bf16);
-  return cudaGetLastError();
+  return launch_with_pdl(kern, dim3(grid), dim3(P_THREADS), PSmem<HD>::BYTES, st, tq, tk, te, p, bf16);
 }
 
 }  // namespace
@@ -1359,9 +1362,8 @@ cudaError_t launch_fam_tc(const void* q, const void* k, const float* lse, int dt
     long long blocks = (rows + 255) / 256;
     if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
     count_launches(1);
-    ext_prep_kernel<<<(unsigned)blocks, 256, 0, st>>>(lse, BHq, s.seq_len, S_pad, p.inv_scale,
-                                                     dtype == KVP_BF16, (uint4*)ext, queue);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_with_pdl(ext_prep_kernel, dim3((unsigned)blocks), dim3(256), 0, st, lse, BHq,
+                                    s.seq_len, S_pad, p.inv_scale, dtype == KVP_BF16, (uint4*)ext, queue);
     if (e != cudaSuccess) return e;
     p.queue = queue;
     p.total_items = (int)items;
@@ -1371,12 +1373,10 @@ cudaError_t launch_fam_tc(const void* q, const void* k, const float* lse, int dt
   }
   count_launches(1);
   if (per_head)
-    fam_reduce_heads_kernel<<<dim3(f.NKT, p.n_groups), BM, 0, st>>>((const float*)ws, s.seq_len, s.h_kv, p.G,
-                                                                    f.NT0, f.TPC, f.CMAX, f.NKT, F);
-  else
-    fam_reduce_kernel<<<dim3(f.NKT, p.n_groups), BM, 0, st>>>((const float*)ws, s.seq_len, f.NT0, f.TPC,
-                                                              f.CMAX, f.NKT, F);
-  return cudaGetLastError();
+    return launch_with_pdl(fam_reduce_heads_kernel, dim3(f.NKT, p.n_groups), dim3(BM), 0, st, (const float*)ws,
+                           s.seq_len, s.h_kv, p.G, f.NT0, f.TPC, f.CMAX, f.NKT, F);
+  return launch_with_pdl(fam_reduce_kernel, dim3(f.NKT, p.n_groups), dim3(BM), 0, st, (const float*)ws, s.seq_len,
+                         f.NT0, f.TPC, f.CMAX, f.NKT, F);
 }
 
 }  // namespace kvp

@@ -3,6 +3,8 @@
 #pragma once
 
 #include <cuda_runtime.h>
+
+#include <utility>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -19,6 +21,23 @@ inline cudaLaunchAttribute pdl_attribute() {
   a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   a.val.programmaticStreamSerializationAllowed = 1;
   return a;
+}
+
+// Launches `kern` with programmatic dependent launch (the kernel must call wait_prior_grid()
+// before it reads what the previous kernel of the stream wrote, or writes what it reads).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_with_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // Shape of a row-LSE / future-mass problem and the element strides of Q and K (batch, head,
