@@ -188,6 +188,28 @@ class L2Flush:
         torch.cuda._sleep(self.HEAD_START_CYCLES)
 
 
+def capture_graph(fn, dev):
+    """fn's launches captured into one CUDA graph (after a warm-up call of fn outside capture),
+    or None when capture fails."""
+    try:
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(dev)
+        s.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(s):
+            fn()
+        torch.cuda.current_stream(dev).wait_stream(s)
+        torch.cuda.synchronize(dev)
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize(dev)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        return g
+    except Exception:                      # noqa: BLE001 -- any capture problem: no graph
+        torch.cuda.synchronize(dev)
+        return None
+
+
 def file_sha(path):
     return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
 
@@ -209,6 +231,42 @@ def oracle_sample_time(w, seconds_hint=None):
     desc = (f"one query head (of {w.h_q}) of the {w.name} layer: full causal row LSE and future "
             f"mass over all {S} keys, fp64 numpy")
     return flops, dt, os.cpu_count(), desc
+
+
+def oracle_eviction_time(n_layers=4):
+    """The oracle's selection, compaction and decode on the Qwen2.5-1.5B decode-eviction shapes at
+    b = 4096, fp64 numpy on the host cores: selection over all 56 rows x 120000 seeded scores;
+    compaction and decode of `n_layers` layers (2 rows each) with 4096 kept rows per row gathered
+    from a cache of 8192 tokens per row (the gather and the decode scale with the kept rows, not
+    with T).  Rates are per the rows each part ran on."""
+    import numpy as np
+    import oracle
+    w = kvp_inputs.QWEN25_15B_DECODE
+    R, T, D, b = w.rows, w.seq_len, w.head_dim, max(w.decode_budgets)
+    scores = kvp_inputs.make_scores(R, T, seed=7).numpy()
+    t0 = time.perf_counter()
+    oracle.select_topk(scores, [b] * R, w.n_sink, w.n_recent, b_max=b)
+    t_sel = time.perf_counter() - t0
+    x = kvp_inputs.make_decode_cache(w, seq_len=2 * b)
+    Rs = n_layers * w.h_kv
+    rng = np.random.default_rng(0)
+    idx = np.stack([np.sort(rng.choice(2 * b, b, replace=False)) for _ in range(Rs)])
+    cnt = np.full(Rs, b)
+    k16 = x["k"][:Rs].view(torch.int16).numpy()
+    v16 = x["v"][:Rs].view(torch.int16).numpy()
+    t0 = time.perf_counter()
+    kc, vc = oracle.compact_kv(k16, v16, idx, cnt)
+    t_cmp = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.decode_attn(x["q"][:n_layers], kc.view(np.float16), vc.view(np.float16), cnt, D ** -0.5)
+    t_dec = time.perf_counter() - t0
+    kv_bytes = 2 * Rs * b * D * 2
+    return {"workload": w.name, "budget": b,
+            "select_topk": {"seconds": t_sel, "GB/s": R * T * 4 / t_sel / 1e9, "rows": R},
+            "compact_kv": {"seconds": t_cmp, "GB/s": 2 * kv_bytes / t_cmp / 1e9, "rows": Rs},
+            "decode_attn": {"seconds": t_dec, "GB/s": kv_bytes / t_dec / 1e9, "rows": Rs},
+            "sample": f"selection of all {R} rows; compaction and decode of {n_layers} layers "
+                      f"({Rs} rows), 4096 kept rows each gathered from an 8192-token cache"}
 
 
 def run_reference(args):
@@ -382,6 +440,12 @@ def run_kvp(args):
         t_1 = oracle_one_thread_time(w)
         if t_1 is not None:
             cpu["one_thread"] = {"value": f_c / t_1 / 1e12, "unit": "TFLOP/s", "seconds": t_1, "cores": 1}
+        # the long-context passes at the oracle's measured rate (not run: hours of CPU time)
+        cpu["extrapolated"] = {lw.name: {"flops": lf, "seconds": lf / (f_c / t_c),
+                                         "note": "extrapolated from the sample's flop rate"}
+                               for lw, lf in ((kvp_inputs.LLAMA31_8B_32L, long_context_flops(kvp_inputs.LLAMA31_8B_32L)),
+                                              (kvp_inputs.QWEN3_8B_131K, long_context_flops(kvp_inputs.QWEN3_8B_131K)))}
+        cpu["decode_eviction"] = oracle_eviction_time()
     clk.__exit__(None, None, None)
     clocks = clk.summary()
     line = {
@@ -535,16 +599,21 @@ def _decode_eviction_budget(kvp, dev, K, W, flush, peaks, w, x, b):
             kvp.kvp_decode_attn(x["q"], ck, cv, cnt, out=out, workspace=ws_pr)
 
     loop()
+    graph = capture_graph(loop, dev)       # replayed as one CUDA graph when capture works
     t_loop = 0.0
     for _ in range(3):
         flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        loop()
+        if graph is not None:
+            graph.replay()
+        else:
+            loop()
         e1.record(stream)
         torch.cuda.synchronize(dev)
         t_loop += e0.elapsed_time(e1) / n_launch / 3
-    del copies
+    graph_used = graph is not None
+    del copies, graph
     kvp.kvp_check_device_status()
     gbs_loop = dec_bytes / (t_loop / 1e3) / 1e9
     gbs_chain = dec_bytes / ((t_chain - t_chain0) / 1e3) / 1e9
@@ -553,7 +622,8 @@ def _decode_eviction_budget(kvp, dev, K, W, flush, peaks, w, x, b):
         "value": gbs_loop, "unit": "GB/s", "frac": gbs_loop / hbm, "peak": hbm,
         "ms": t_loop, "bytes": dec_bytes,
         "timing": f"decode loop: {n_launch} launches back to back over {n_c} rotated copies of the "
-                  f"pruned cache ({n_c * cache_bytes / 1e6:.0f} MB > L2), average per launch",
+                  f"pruned cache ({n_c * cache_bytes / 1e6:.0f} MB > L2), average per launch"
+                  + (", replayed as one CUDA graph" if graph_used else ""),
         "isolated": {"value": gbs, "frac": gbs / hbm, "ms": t_dec,
                      "l2": "flushed before the one timed launch"},
         "eviction_step_chain": {"select_compact_decode_ms": t_chain, "select_compact_ms": t_chain0,
@@ -566,6 +636,12 @@ def _decode_eviction_budget(kvp, dev, K, W, flush, peaks, w, x, b):
             "compact_kv": {"ms": t_cmp, "GB/s": cmp_bytes / (t_cmp / 1e3) / 1e9},
         },
     }
+
+
+def long_context_flops(w):
+    """A1 + A2 flops of a long-context workload: 2*D*H_q*[S(S+1)/2 + (S-w)(S-w+1)/2] per layer."""
+    S, ww = w.seq_len, max(w.seq_len - w.window, 0)
+    return w.n_layers * 2.0 * w.head_dim * w.h_q * (S * (S + 1) // 2 + ww * (ww + 1) // 2)
 
 
 def long_context_measure(kvp, dev, W, peaks, K=3):
