@@ -599,20 +599,22 @@ def _decode_eviction_budget(kvp, dev, K, W, flush, peaks, w, x, b):
             kvp.kvp_decode_attn(x["q"], ck, cv, cnt, out=out, workspace=ws_pr)
 
     loop()
-    graph = capture_graph(loop, dev)       # replayed as one CUDA graph when capture works
-    t_loop = 0.0
-    for _ in range(3):
-        flush()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        if graph is not None:
-            graph.replay()
-        else:
-            loop()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        t_loop += e0.elapsed_time(e1) / n_launch / 3
-    graph_used = graph is not None
+    graph = capture_graph(loop, dev)       # the same loop as one CUDA graph, when capture works
+
+    def timed(run):
+        t = 0.0
+        for _ in range(3):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            run()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            t += e0.elapsed_time(e1) / n_launch / 3
+        return t
+
+    t_loop = timed(loop)
+    t_graph = timed(graph.replay) if graph is not None else None
     del copies, graph
     kvp.kvp_check_device_status()
     gbs_loop = dec_bytes / (t_loop / 1e3) / 1e9
@@ -622,8 +624,10 @@ def _decode_eviction_budget(kvp, dev, K, W, flush, peaks, w, x, b):
         "value": gbs_loop, "unit": "GB/s", "frac": gbs_loop / hbm, "peak": hbm,
         "ms": t_loop, "bytes": dec_bytes,
         "timing": f"decode loop: {n_launch} launches back to back over {n_c} rotated copies of the "
-                  f"pruned cache ({n_c * cache_bytes / 1e6:.0f} MB > L2), average per launch"
-                  + (", replayed as one CUDA graph" if graph_used else ""),
+                  f"pruned cache ({n_c * cache_bytes / 1e6:.0f} MB > L2), average per launch",
+        "graph_replay": None if t_graph is None else {
+            "ms": t_graph, "value": dec_bytes / (t_graph / 1e3) / 1e9,
+            "frac": dec_bytes / (t_graph / 1e3) / 1e9 / hbm, "note": "the same loop captured as one CUDA graph"},
         "isolated": {"value": gbs, "frac": gbs / hbm, "ms": t_dec,
                      "l2": "flushed before the one timed launch"},
         "eviction_step_chain": {"select_compact_decode_ms": t_chain, "select_compact_ms": t_chain0,
