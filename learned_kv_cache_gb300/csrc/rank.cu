@@ -44,6 +44,7 @@ __global__ void __launch_bounds__(RK_THREADS) rank_hist_kernel(const float* __re
                                                               const uint32_t* __restrict__ keys,
                                                               int first, int T, int NB, int shift,
                                                               int* __restrict__ hist) {
+  wait_prior_grid();
   __shared__ int h[256];
   const int b = blockIdx.x, r = blockIdx.y, tid = threadIdx.x;
   h[tid] = 0;
@@ -60,6 +61,7 @@ __global__ void __launch_bounds__(RK_THREADS) rank_hist_kernel(const float* __re
 
 // hist[r][b][d] (counts) -> global start of (tile b, digit d) in row r's sorted order.
 __global__ void __launch_bounds__(256) rank_scan_kernel(int NB, int* __restrict__ hist) {
+  wait_prior_grid();
   __shared__ int tot[256];
   const int r = blockIdx.x, d = threadIdx.x;
   int* hr = hist + (size_t)r * NB * 256;
@@ -85,6 +87,7 @@ __global__ void __launch_bounds__(RK_THREADS) rank_scatter_kernel(
     const float* __restrict__ scores, const uint32_t* __restrict__ keys_in,
     const int32_t* __restrict__ vals_in, int first, int T, int NB, int shift,
     const int* __restrict__ hist, uint32_t* __restrict__ keys_out, int32_t* __restrict__ vals_out) {
+  wait_prior_grid();
   __shared__ int start[256];                 // global position of the tile's next entry per digit
   __shared__ int wcnt[RK_WARPS][256];        // per-round counts of each warp
   const int b = blockIdx.x, r = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -123,6 +126,7 @@ __global__ void __launch_bounds__(RK_THREADS) rank_scatter_kernel(
 
 __global__ void rank_invert_kernel(const int32_t* __restrict__ vals, int R, int T,
                                    int32_t* __restrict__ ranks, int* status) {
+  wait_prior_grid();
   const long long total = (long long)R * T;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
@@ -158,6 +162,7 @@ __global__ void __launch_bounds__(AUC_THREADS) auc_partial_kernel(const float* _
                                                                   const int32_t* __restrict__ ranks,
                                                                   int M, int T, int NC, int vec,
                                                                   double* __restrict__ part) {
+  wait_prior_grid();
   __shared__ double red[AUC_THREADS / 32];
   const int c = blockIdx.x, m = blockIdx.y, r = blockIdx.z, tid = threadIdx.x;
   const float* f = F + (size_t)r * T;
@@ -223,6 +228,7 @@ __global__ void __launch_bounds__(AUC_THREADS) auc_partial_kernel(const float* _
 
 __global__ void auc_reduce_kernel(const double* __restrict__ part, int RM, int NC,
                                   double* __restrict__ auc) {
+  wait_prior_grid();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= RM) return;
   double s = 0.0;
@@ -258,9 +264,13 @@ cudaError_t launch_rank_rows(const float* scores, int R, int T, int32_t* ranks, 
   for (int pass = 0; pass < 4; ++pass) {
     const int first = pass == 0, shift = 8 * pass;
     count_launches(3);
-    rank_hist_kernel<<<grid, RK_THREADS, 0, st>>>(scores, kin, first, T, NB, shift, hist);
-    rank_scan_kernel<<<R, 256, 0, st>>>(NB, hist);
-    rank_scatter_kernel<<<grid, RK_THREADS, 0, st>>>(scores, kin, vin, first, T, NB, shift, hist, kout, vout);
+    cudaError_t e = launch_with_pdl(rank_hist_kernel, grid, dim3(RK_THREADS), 0, st, scores, kin, first, T, NB,
+                                    shift, hist);
+    if (e == cudaSuccess) e = launch_with_pdl(rank_scan_kernel, dim3(R), dim3(256), 0, st, NB, hist);
+    if (e == cudaSuccess)
+      e = launch_with_pdl(rank_scatter_kernel, grid, dim3(RK_THREADS), 0, st, scores, kin, vin, first, T, NB, shift,
+                          hist, kout, vout);
+    if (e != cudaSuccess) return e;
     kin = kout;
     vin = vout;
     kout = kout == ka ? kb : ka;
@@ -272,8 +282,7 @@ cudaError_t launch_rank_rows(const float* scores, int R, int T, int32_t* ranks, 
   long long blocks = ((long long)n + 255) / 256;
   if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
   count_launches(1);
-  rank_invert_kernel<<<(unsigned)blocks, 256, 0, st>>>(vin, R, T, ranks, status);
-  return cudaGetLastError();
+  return launch_with_pdl(rank_invert_kernel, dim3((unsigned)blocks), dim3(256), 0, st, vin, R, T, ranks, status);
 }
 
 size_t eviction_auc_workspace_size(int R, int M, int T) {
@@ -287,10 +296,12 @@ cudaError_t launch_eviction_auc(const float* F, const int32_t* ranks, int R, int
   const int vec = T % 4 == 0 && ((uintptr_t)F & 15) == 0 && ((uintptr_t)ranks & 15) == 0;
   double* part = (double*)ws;
   count_launches(2);
-  auc_partial_kernel<<<dim3(NC, M, R), AUC_THREADS, 0, st>>>(F, ranks, M, T, NC, vec, part);
+  cudaError_t e = launch_with_pdl(auc_partial_kernel, dim3(NC, M, R), dim3(AUC_THREADS), 0, st, F, ranks, M, T, NC,
+                                  vec, part);
+  if (e != cudaSuccess) return e;
   const int RM = R * M;
-  auc_reduce_kernel<<<(RM + 255) / 256, 256, 0, st>>>(part, RM, NC, auc);
-  return cudaGetLastError();
+  return launch_with_pdl(auc_reduce_kernel, dim3((RM + 255) / 256), dim3(256), 0, st, (const double*)part, RM, NC,
+                         auc);
 }
 
 }  // namespace kvp
