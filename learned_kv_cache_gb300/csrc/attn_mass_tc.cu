@@ -317,6 +317,7 @@ __global__ void __launch_bounds__(Epi<MODE>::THREADS, 2)
     }
     ptx::fence_proxy_async_smem();
   }
+  wait_prior_grid();                     // (sparse pass) the rank-ordered keys come from the kernel before
   int* tau_red = reinterpret_cast<int*>(smem + L::OFF_MISC + 16);      // sparse pass: [4] max, [4] min
   if (MODE == 2 && p.inv != nullptr && warp < 4) {
     // cutoff range over the query tile's rows (rows past S ignored)
@@ -1036,6 +1037,7 @@ __global__ void rank_scatter_keys_kernel(const uint16_t* __restrict__ k, long lo
                                          long long k_sr, int Hkv, const int32_t* __restrict__ ranks,
                                          int S, int vpr, long long total, int32_t* __restrict__ inv,
                                          uint4* __restrict__ ks, int* ok) {
+  wait_prior_grid();
   for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
        e += (long long)gridDim.x * blockDim.x) {
     const long long hj = e / vpr;                    // h * S + j, h = b * Hkv + hk
@@ -1191,6 +1193,8 @@ cudaError_t launch_tc_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<HD>::BYTES);
   if (e != cudaSuccess) return e;
   count_launches(1);
+  if (MODE == 2 && p.inv != nullptr)       // after its preparation scatter: dependent launch
+    return launch_with_pdl(kern, dim3(grid), dim3(Epi<MODE>::THREADS), Smem<HD>::BYTES, st, tq, tk, te, p, bf16);
   kern<<<grid, Epi<MODE>::THREADS, Smem<HD>::BYTES, st>>>(tq, tk, te, p, bf16);
   return cudaGetLastError();
 }
