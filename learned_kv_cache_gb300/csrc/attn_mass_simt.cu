@@ -222,6 +222,7 @@ __global__ void __launch_bounds__(256) fam_simt_kernel(const T* __restrict__ q,
 __global__ void target_epilogue_kernel(const float* __restrict__ Fh, int Hq, int Hkv, int S, int w,
                                        float eps, int aggregate, float* __restrict__ target,
                                        float* __restrict__ F, long long total) {
+  wait_prior_grid();                     // the per-head sums come from the kernel just before
   const int G = Hq / Hkv;
   for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
        e += (long long)gridDim.x * blockDim.x) {
@@ -291,9 +292,8 @@ cudaError_t launch_target_epilogue(const float* F_heads, int n_batch, int h_q, i
   long long blocks = (total + 255) / 256;
   if (blocks > 4096) blocks = 4096;
   count_launches(1);
-  target_epilogue_kernel<<<(unsigned)blocks, 256, 0, st>>>(F_heads, h_q, h_kv, S, window, eps, aggregate,
-                                                           target, F, total);
-  return cudaGetLastError();
+  return launch_with_pdl(target_epilogue_kernel, dim3((unsigned)blocks), dim3(256), 0, st, F_heads, h_q, h_kv, S,
+                         window, eps, aggregate, target, F, total);
 }
 
 }  // namespace kvp
