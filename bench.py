@@ -51,8 +51,8 @@ NCU_TRAFFIC = {
     # ncu --set full of the mass pass (mass_tc_persistent_kernel) and the row LSE pass
     # (attn_tc_kernel<0>) on the benchmark layer (S = 8192; the kernel source hashed below),
     # DRAM bytes read + written per launch
-    "future_attn_mass": {"sha": "00ee4da619f9519e", "bytes": 115552256 + 3821568},
-    "lse_pass": {"sha": "00ee4da619f9519e", "bytes": 83914496 + 2335232},
+    "future_attn_mass": {"sha": "8cc03e9b61739b38", "bytes": 119132416 + 3770368},
+    "lse_pass": {"sha": "8cc03e9b61739b38", "bytes": 83915264 + 2302208},
 }
 
 
