@@ -46,6 +46,8 @@ class PrefillPrunePlan:
         self._dev_in = None
         self._copy_stream = None
         self._mass_stream = None
+        # run_from_host: KV heads per copy slice (they must add up to h_kv); None = four equal slices
+        self.kv_slices = None
 
     def __call__(self, q, k, v, dq, budgets, stream=None):
         R = self.B * self.Hkv
@@ -77,8 +79,15 @@ class PrefillPrunePlan:
         B, Hq, Hkv, S, D = self.B, self.Hq, self.Hkv, self.S, self.D
         G = Hq // Hkv
         R = B * Hkv
-        gs = max(1, Hkv // 4)                     # KV heads per slice
-        slices = [(b, h0, min(Hkv, h0 + gs)) for b in range(B) for h0 in range(0, Hkv, gs)]
+        if self.kv_slices is None:
+            gs = max(1, Hkv // 4)                 # KV heads per slice
+            widths = [min(gs, Hkv - h0) for h0 in range(0, Hkv, gs)]
+        else:
+            widths = [int(x) for x in self.kv_slices]
+            if sum(widths) != Hkv or min(widths) < 1:
+                raise ValueError(f"kv_slices {widths} must be positive and add up to h_kv = {Hkv}")
+        bounds = [sum(widths[:i]) for i in range(len(widths) + 1)]
+        slices = [(b, bounds[i], bounds[i + 1]) for b in range(B) for i in range(len(widths))]
         ready = []
         with torch.cuda.stream(cs):
             for b, h0, h1 in slices:
