@@ -36,3 +36,15 @@ def test_reference_arm_other_ranks_print_nothing():
     r = _run({"WORLD_SIZE": "2", "RANK": "1", "LOCAL_RANK": "1"})
     assert r.returncode == 0, r.stderr[-2000:]
     assert not [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+
+
+def test_long_context_flops_match_the_workloads():
+    """The long-context legs count 2*D*H_q*[S(S+1)/2 + (S-w)(S-w+1)/2] per layer, the same
+    algorithmic flops as the workload definitions (2.81e14 and 1.405e14)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import kvp_inputs
+    for w, want in ((kvp_inputs.LLAMA31_8B_32L, 2.809e14), (kvp_inputs.QWEN3_8B_131K, 1.405e14)):
+        f = bench.long_context_flops(w)
+        assert f == w.attn_mass_flops()
+        assert abs(f - want) / want < 1e-3
