@@ -1097,6 +1097,39 @@ __global__ void __launch_bounds__(BM) fam_reduce_heads_kernel(const float* __res
   }
 }
 
+// KVpop target straight from the per-head partial sums: fam_reduce_heads_kernel and the target
+// epilogue in one pass with the same arithmetic -- each query head's sum over its chunks and
+// slots in order, N_t = max(1, S - (j + w)), then the group max of log(eps + F_g / N_t) or
+// log(eps + sum_g F_g / (N_t G)); F_heads, target and F each written when given.
+__global__ void __launch_bounds__(BM) fam_target_kernel(const float* __restrict__ part, int S, int Hkv, int G,
+                                                        int NT0, int TPC, int CMAX, int NKT, int window,
+                                                        float eps, int aggregate, float* __restrict__ F_heads,
+                                                        float* __restrict__ target, float* __restrict__ F) {
+  wait_prior_grid();
+  const int jt = blockIdx.x, group = blockIdx.y, r = threadIdx.x;
+  const int j = jt * BM + r;
+  if (j >= S) return;
+  const int nt = max(0, NT0 - jt);
+  const int nch = (nt + TPC - 1) / TPC;
+  const int b = group / Hkv, h = group % Hkv;
+  const float N = (float)max(1, S - (j + window));
+  float sum = 0.f, best = -INFINITY;
+  for (int g = 0; g < G; ++g) {
+    float f = 0.f;
+    for (int c = 0; c < nch; ++c) {
+      const float* src = part + ((((size_t)group * NKT + jt) * CMAX + c) * G + g) * P_SLOTS * BM + r;
+#pragma unroll
+      for (int q = 0; q < P_SLOTS; ++q) f += src[(size_t)q * BM];
+    }
+    if (F_heads) F_heads[((size_t)b * Hkv * G + h * G + g) * S + j] = f;
+    sum += f;
+    best = fmaxf(best, logf(eps + f / N));
+  }
+  const size_t e = (size_t)group * S + j;
+  if (target) target[e] = aggregate == 0 ? best : logf(eps + sum / (N * (float)G));
+  if (F) F[e] = sum;
+}
+
 // ---------------------------------------------------------------- host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -1333,7 +1366,7 @@ cudaError_t launch_lse_tc(const void* q, const void* k, int dtype, AttnShape s, 
 
 cudaError_t launch_fam_tc(const void* q, const void* k, const float* lse, int dtype, AttnShape s,
                           float scale, int window, float* F, void* ws, size_t ws_bytes, int* status,
-                          cudaStream_t st, int per_head) {
+                          cudaStream_t st, int per_head, const TargetOut* tgt) {
   const FamSched f = fam_schedule(s, window);
   if (ws_bytes < fam_tc_workspace_size(s, window, per_head)) return cudaErrorInvalidValue;
   TcParams p{};
@@ -1389,6 +1422,10 @@ cudaError_t launch_fam_tc(const void* q, const void* k, const float* lse, int dt
     if (e != cudaSuccess) return e;
   }
   count_launches(1);
+  if (per_head && tgt)
+    return launch_with_pdl(fam_target_kernel, dim3(f.NKT, p.n_groups), dim3(BM), 0, st, (const float*)ws,
+                           s.seq_len, s.h_kv, p.G, f.NT0, f.TPC, f.CMAX, f.NKT, window, tgt->eps, tgt->aggregate,
+                           F, tgt->target, tgt->F);
   if (per_head)
     return launch_with_pdl(fam_reduce_heads_kernel, dim3(f.NKT, p.n_groups), dim3(BM), 0, st, (const float*)ws,
                            s.seq_len, s.h_kv, p.G, f.NT0, f.TPC, f.CMAX, f.NKT, F);

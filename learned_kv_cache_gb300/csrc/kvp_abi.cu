@@ -351,13 +351,18 @@ int kvp_future_attn_target(const void* q, const void* k, const float* lse, int d
   if (((uintptr_t)workspace & 255u) != 0) return fail(KVP_ERR_INVALID_ARG, "workspace not 256-byte aligned");
   int* st = nullptr;
   KVP_TRY(status_ptr(&st));
-  float* heads = F_heads ? F_heads : (float*)workspace;
   char* part = (char*)workspace + target_heads_bytes(n_batch, h_q, seq_len);
-  cudaError_t e = tc ? kvp::launch_fam_tc(q, k, lse, dtype, s, sm_scale, window, heads, part,
-                                          workspace_bytes - target_heads_bytes(n_batch, h_q, seq_len), st,
-                                          (cudaStream_t)stream, 1)
-                     : kvp::launch_fam_simt(q, k, lse, dtype, s, sm_scale, window, heads,
-                                            (cudaStream_t)stream, 1);
+  if (tc) {
+    // the per-head sums go straight into the target (and F_heads / F when asked for)
+    const kvp::TargetOut to{eps, aggregate, target, F};
+    cudaError_t e = kvp::launch_fam_tc(q, k, lse, dtype, s, sm_scale, window, F_heads, part,
+                                       workspace_bytes - target_heads_bytes(n_batch, h_q, seq_len), st,
+                                       (cudaStream_t)stream, 1, &to);
+    if (e != cudaSuccess) return cuda_fail(e, "kvp_future_attn_target launch");
+    return KVP_OK;
+  }
+  float* heads = F_heads ? F_heads : (float*)workspace;
+  cudaError_t e = kvp::launch_fam_simt(q, k, lse, dtype, s, sm_scale, window, heads, (cudaStream_t)stream, 1);
   if (e != cudaSuccess) return cuda_fail(e, "kvp_future_attn_target launch");
   if (target || F) {
     e = kvp::launch_target_epilogue(heads, n_batch, h_q, h_kv, seq_len, window, eps, aggregate, target, F,

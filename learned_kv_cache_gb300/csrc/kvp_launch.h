@@ -84,10 +84,19 @@ size_t fam_tc_workspace_size(AttnShape s, int window, int per_head = 0);
 // mask == null: the dense row LSE; mask != null: the sparse row LSE.
 cudaError_t launch_lse_tc(const void* q, const void* k, int dtype, AttnShape s, float scale,
                           float* lse, int* status, cudaStream_t st, const SparseMask* mask = nullptr);
-// per_head = 1: F receives each query head's mass, [n_batch, h_q, seq_len].
+// KVpop target outputs computed straight from the per-head partial sums (per_head = 1): N_t,
+// log(eps + m), group max or probability-space mean; target and F nullable.
+struct TargetOut {
+  float eps;
+  int aggregate;
+  float* target;   // [n_batch, h_kv, seq_len]
+  float* F;        // [n_batch, h_kv, seq_len]
+};
+// per_head = 1: F receives each query head's mass, [n_batch, h_q, seq_len] (nullable when tgt is
+// given).
 cudaError_t launch_fam_tc(const void* q, const void* k, const float* lse, int dtype, AttnShape s,
                           float scale, int window, float* F, void* ws, size_t ws_bytes,
-                          int* status, cudaStream_t st, int per_head = 0);
+                          int* status, cudaStream_t st, int per_head = 0, const TargetOut* tgt = nullptr);
 
 cudaError_t launch_soft_topk(const double* x, int n, double k, int t, double* ratios,
                              int32_t* budgets, cudaStream_t st);
