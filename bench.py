@@ -51,8 +51,8 @@ NCU_TRAFFIC = {
     # ncu --set full of the mass pass (mass_tc_persistent_kernel) and the row LSE pass
     # (attn_tc_kernel<0>) on the benchmark layer (S = 8192; the kernel source hashed below),
     # DRAM bytes read + written per launch
-    "future_attn_mass": {"sha": "c9ac2cc24dbfaec6", "bytes": 113908736 + 3802112},
-    "lse_pass": {"sha": "c9ac2cc24dbfaec6", "bytes": 83920640 + 2452480},
+    "future_attn_mass": {"sha": "283da76505b05544", "bytes": 112800000 + 3699456},
+    "lse_pass": {"sha": "283da76505b05544", "bytes": 83914496 + 2318336},
 }
 
 
