@@ -51,8 +51,8 @@ NCU_TRAFFIC = {
     # ncu --set full of the mass pass (mass_tc_persistent_kernel) and the row LSE pass
     # (attn_tc_kernel<0>) on the benchmark layer (S = 8192; the kernel source hashed below),
     # DRAM bytes read + written per launch
-    "future_attn_mass": {"sha": "283da76505b05544", "bytes": 112800000 + 3699456},
-    "lse_pass": {"sha": "283da76505b05544", "bytes": 83914496 + 2318336},
+    "future_attn_mass": {"sha": "5b69551d3fb6cae3", "bytes": 115430144 + 3844096},
+    "lse_pass": {"sha": "5b69551d3fb6cae3", "bytes": 83915008 + 2474752},
 }
 
 

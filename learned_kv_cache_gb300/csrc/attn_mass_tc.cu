@@ -1074,33 +1074,10 @@ __global__ void __launch_bounds__(BM) fam_reduce_kernel(const float* __restrict_
   F[(size_t)group * S + j] = f;
 }
 
-// F_heads[b, h*G + g, j] = query head g's partial sums of key tile j/128 (chunks in order, the
-// two slots of each in order).
-__global__ void __launch_bounds__(BM) fam_reduce_heads_kernel(const float* __restrict__ part, int S, int Hkv,
-                                                              int G, int NT0, int TPC, int CMAX, int NKT,
-                                                              float* __restrict__ F_heads) {
-  wait_prior_grid();
-  const int jt = blockIdx.x, group = blockIdx.y, r = threadIdx.x;
-  const int j = jt * BM + r;
-  if (j >= S) return;
-  const int nt = max(0, NT0 - jt);
-  const int nch = (nt + TPC - 1) / TPC;
-  const int b = group / Hkv, h = group % Hkv;
-  for (int g = 0; g < G; ++g) {
-    float f = 0.f;
-    for (int c = 0; c < nch; ++c) {
-      const float* src = part + ((((size_t)group * NKT + jt) * CMAX + c) * G + g) * P_SLOTS * BM + r;
-#pragma unroll
-      for (int q = 0; q < P_SLOTS; ++q) f += src[(size_t)q * BM];
-    }
-    F_heads[((size_t)b * Hkv * G + h * G + g) * S + j] = f;
-  }
-}
-
-// KVpop target straight from the per-head partial sums: fam_reduce_heads_kernel and the target
-// epilogue in one pass with the same arithmetic -- each query head's sum over its chunks and
-// slots in order, N_t = max(1, S - (j + w)), then the group max of log(eps + F_g / N_t) or
-// log(eps + sum_g F_g / (N_t G)); F_heads, target and F each written when given.
+// Per-head mode of the mass pass, reduce and KVpop target in one pass: each query head's sum
+// over its chunks and slots in order (F_heads), then N_t = max(1, S - (j + w)) and the group max
+// of log(eps + F_g / N_t) or log(eps + sum_g F_g / (N_t G)) (target), and the group sum (F);
+// each written when given.  The arithmetic of the target is that of target_epilogue_kernel.
 __global__ void __launch_bounds__(BM) fam_target_kernel(const float* __restrict__ part, int S, int Hkv, int G,
                                                         int NT0, int TPC, int CMAX, int NKT, int window,
                                                         float eps, int aggregate, float* __restrict__ F_heads,
@@ -1422,13 +1399,13 @@ cudaError_t launch_fam_tc(const void* q, const void* k, const float* lse, int dt
     if (e != cudaSuccess) return e;
   }
   count_launches(1);
-  if (per_head && tgt)
+  if (per_head) {                          // the per-head sums (and the target when asked for)
+    const TargetOut none{0.f, 0, nullptr, nullptr};
+    const TargetOut* t = tgt ? tgt : &none;
     return launch_with_pdl(fam_target_kernel, dim3(f.NKT, p.n_groups), dim3(BM), 0, st, (const float*)ws,
-                           s.seq_len, s.h_kv, p.G, f.NT0, f.TPC, f.CMAX, f.NKT, window, tgt->eps, tgt->aggregate,
-                           F, tgt->target, tgt->F);
-  if (per_head)
-    return launch_with_pdl(fam_reduce_heads_kernel, dim3(f.NKT, p.n_groups), dim3(BM), 0, st, (const float*)ws,
-                           s.seq_len, s.h_kv, p.G, f.NT0, f.TPC, f.CMAX, f.NKT, F);
+                           s.seq_len, s.h_kv, p.G, f.NT0, f.TPC, f.CMAX, f.NKT, window, t->eps, t->aggregate,
+                           F, t->target, t->F);
+  }
   return launch_with_pdl(fam_reduce_kernel, dim3(f.NKT, p.n_groups), dim3(BM), 0, st, (const float*)ws, s.seq_len,
                          f.NT0, f.TPC, f.CMAX, f.NKT, F);
 }
